@@ -1,0 +1,423 @@
+"""Benchmark: attention-backward TFLOP/s of the varlen (TND) backward on GB300.
+
+One step = one fa_varlen_bwd call over the whole workload: the host
+schedule and its upload, the preprocess kernel, the main backward kernel and
+the dQ convert kernel.  FLOPs are counted as 5 * 2 * D per allowed
+(query, key) pair per head (the five dense contractions of the backward).
+
+Default workload: bf16 TND, lengths [512, 1024, 2048, 512] (T = 4096),
+N = 16, D = 128, causal, scale 1/sqrt(128); Q, K, V, dY ~ N(0, 1) from seed 0.
+Its inputs fit in L2, so L2 is flushed (a 256 MB write) before every timed
+step, outside the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5]
+                    [--impl reference]
+
+`--impl reference` times the fp64 CPU oracle on a bounded sample of the same
+workload instead (the only reference available: the pages ship no code).
+Under torchrun (N > 1) every rank runs the workload on its own GPU (weak
+scaling, no data-path collective); rank 0 prints the JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention-backward TFLOP/s (bf16 varlen causal) and % of GB300 dense BF16 peak"
+UNIT = "TFLOP/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def allowed_pairs(lens_q, lens_kv, pre, nxt) -> int:
+    """Exact count of allowed (i, j) pairs of one head: sum over rows of the
+    window [i - pre, i + next] clipped to [0, Lk)."""
+    total = 0
+    for lq, lk in zip(lens_q, lens_kv):
+        if lq == 0 or lk == 0:
+            continue
+        i = np.arange(lq, dtype=np.int64)
+        lo = np.maximum(0, i - pre)
+        hi = np.minimum(lk - 1, i + nxt)
+        total += int(np.maximum(0, hi - lo + 1).sum())
+    return total
+
+
+def workload_flops(w) -> float:
+    return 10.0 * w.head_dim * w.n_heads * allowed_pairs(w.lens, w.lens_kv, w.pre_tokens,
+                                                         w.next_tokens)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Max of a per-rank number over all ranks (timing only, never data)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def profile_traffic(kernel_tag: str, source_digest: str):
+    """DRAM bytes per launch of the main kernel from the committed ncu summary,
+    or None when absent or taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    d = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
+    if not m or not d or d.group(1) != source_digest:
+        return None
+    return float(m.group(1))
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "varlen_flashattention_backward_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+# ---------------------------------------------------------------------------
+# the oracle arm (CPU)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w, tensors, budget_s: float):
+    """Times the fp64 oracle (forward + backward, as it stands) on whole
+    (sequence, head) units of the workload, longest sequence first, until
+    `budget_s` seconds of work.  Returns (seconds, flops, description)."""
+    import oracle
+    q, k, v, dy = (t.double().numpy() for t in tensors)
+    cq, ck = oracle.cu_seqlens(w.lens), oracle.cu_seqlens(w.lens_kv)
+    order = sorted(range(len(w.lens)), key=lambda b: -w.lens[b])
+    done, flops, secs = [], 0.0, 0.0
+    group = w.n_heads // w.n_heads_kv
+    for b in order:
+        for n in range(w.n_heads):
+            if secs >= budget_s:
+                break
+            qs, dys = q[cq[b]:cq[b + 1], n], dy[cq[b]:cq[b + 1], n]
+            ks, vs = k[ck[b]:ck[b + 1], n // group], v[ck[b]:ck[b + 1], n // group]
+            t0 = time.perf_counter()
+            y, m, l = oracle.unit_forward(qs, ks, vs, w.scale, w.pre_tokens, w.next_tokens)
+            oracle.unit_backward(qs, ks, vs, dys, y, m, l, w.scale, w.pre_tokens, w.next_tokens)
+            secs += time.perf_counter() - t0
+            flops += 10.0 * w.head_dim * allowed_pairs([w.lens[b]], [w.lens_kv[b]],
+                                                       w.pre_tokens, w.next_tokens)
+            done.append((b, n))
+        if secs >= budget_s:
+            break
+    desc = (f"{len(done)} whole (sequence, head) units of the workload, longest sequence first "
+            f"(lengths {sorted({w.lens[b] for b, _ in done})}), fp64 numpy forward+backward")
+    return secs, flops, desc
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from varlen_flashattention_backward_gb300 import workloads as wl
+    tensors = wl.make_tensors(w)
+    per_step = []
+    # keep the whole run to about two minutes of CPU work
+    budget = min(args.ref_budget, 120.0 / (args.steps + 0.25 * args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(w, tensors, budget / 4)
+    desc = ""
+    for _ in range(args.steps):
+        secs, flops, desc = oracle_sample(w, tensors, budget)
+        per_step.append((secs, flops))
+    secs = sum(s for s, _ in per_step)
+    flops = sum(f for _, f in per_step)
+    value = flops / secs / 1e12
+    cores = cpu_cores()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.describe(), "seed": w.seed},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# the CUDA arm
+# ---------------------------------------------------------------------------
+
+def run_cuda(args, w):
+    import torch
+    from varlen_flashattention_backward_gb300 import binding as fa
+    from varlen_flashattention_backward_gb300 import build as fb
+    from varlen_flashattention_backward_gb300 import workloads as wl
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fb.build()
+    fa.lib()
+
+    tensors = wl.make_tensors(w)
+    q, k, v, dy = (t.to(dev) for t in tensors)
+    mask = None
+    if w.keep_prob < 1.0:
+        mask = fa.gen_keep_mask(w.mask_bits, w.mask_seed, w.keep_prob, device=dev)
+    y, smax, ssum = fa.fwd(q, k, v, w.lens, w.lens_kv, w.scale, w.pre_tokens, w.next_tokens,
+                           w.keep_prob, mask)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    impl = {"auto": fa.FA_BWD_AUTO, "simt": fa.FA_BWD_SIMT, "tcgen05": fa.FA_BWD_TCGEN05}[args.kernel]
+    ws_bytes = fa.bwd_workspace_size(w.lens, w.lens_kv, w.n_heads, w.n_heads_kv, w.head_dim,
+                                     q.dtype, w.keep_prob, w.pre_tokens, w.next_tokens, impl)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(events=None):
+        fa.bwd(q, k, v, dy, y, smax, ssum, w.lens, w.lens_kv, w.scale, w.pre_tokens,
+               w.next_tokens, w.keep_prob, mask, dq=dq, dk=dk, dv=dv, workspace=ws,
+               stream=stream, impl=impl, events=events)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    # per step: [outer start, pre start, main start, main end, convert end, outer end]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    for e in evs:                      # make every event exist before handing it to C
+        for x in e:
+            x.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for e in evs:
+            flush.zero_()
+            e[0].record(stream)
+            step(events=e[1:5])
+            e[5].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    step_ms = [e[0].elapsed_time(e[5]) for e in evs]
+    main_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    pre_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    conv_ms = [e[3].elapsed_time(e[4]) for e in evs]
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    flops = workload_flops(w)
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host inputs -> device, the
+    # backward, device -> pinned host outputs, every step.
+    host_in = [t.cpu().pin_memory() for t in (q, k, v, dy, y, smax, ssum)]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
+    dev_in = [torch.empty_like(t) for t in (q, k, v, dy, y, smax, ssum)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    if mask is not None:
+        host_mask = mask.cpu().pin_memory()
+        dev_mask = torch.empty_like(mask)
+        h2d += host_mask.numel()
+
+    def e2e_step():
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        m = None
+        if mask is not None:
+            dev_mask.copy_(host_mask, non_blocking=True)
+            m = dev_mask
+        a, b_, c = fa.bwd(*dev_in[:4], dev_in[4], dev_in[5], dev_in[6], w.lens, w.lens_kv,
+                          w.scale, w.pre_tokens, w.next_tokens, w.keep_prob, m, dq=dq, dk=dk,
+                          dv=dv, workspace=ws, stream=stream, impl=impl)
+        for h, d in zip(host_out, (a, b_, c)):
+            h.copy_(d, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e_value = world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks["bf16_tflops"])
+    main_avg = sum(main_ms) / len(main_ms)
+    achieved = flops / (main_avg * 1e-3) / 1e12
+    kernel_tag = {fa.FA_BWD_SIMT: "bwd_simt", fa.FA_BWD_TCGEN05: "bwd_tcgen05"}.get(
+        impl, "bwd_tcgen05" if w.dtype != "fp32" else "bwd_simt")
+    traffic = profile_traffic(f"{kernel_tag}_w{w.cid}", source_digest())
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        secs, cflops, desc = oracle_sample(w, tensors, args.ref_budget)
+        cpu = {"value": cflops / secs / 1e12, "unit": UNIT, "cores": cpu_cores(),
+               "kind": "oracle", "sample": desc}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.describe(), "seed": w.seed, "flops_per_step": flops,
+                   "l2": "flushed (256 MB write) before every timed step",
+                   "kernel": args.kernel,
+                   "pct_of_bf16_peak": 100.0 * value / peak},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16_tflops (burst)",
+                     "kernel": kernel_tag, "kernel_ms": main_avg},
+        "kernel_ms": {"preprocess": sum(pre_ms) / len(pre_ms), "main": main_avg,
+                      "dq_convert": sum(conv_ms) / len(conv_ms)},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tcgen05"])
+    ap.add_argument("--ref-budget", type=float, default=10.0,
+                    help="seconds of oracle work per timed sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)          # timing rule: at least 3 warm-up steps
+    from varlen_flashattention_backward_gb300 import workloads as wl
+    w = wl.workload(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_cuda(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

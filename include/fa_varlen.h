@@ -1,0 +1,212 @@
+/*
+ * fa_varlen.h -- C ABI of the GB300 (sm_103a) varlen attention library.
+ *
+ * Operation.  Packed variable-length scaled-dot-product attention in TND
+ * layout, as defined by the web page "CANN/ops-transformer FlashAttention梯度V2"
+ * (aclnnFlashAttentionUnpaddingScoreGradV2), section 功能说明 / 计算公式
+ * (function description / formulas):
+ *
+ *     S  = Mask(scale * Q K^T)            P = Dropout(Softmax(S), keep_prob)
+ *     Y  = P V
+ *     dV = P^T dY      dQ = scale * dS K      dK = scale * dS^T Q
+ *
+ * with dS = P * (dP * Z / keep_prob - D), dP = dY V^T, D_i = sum_d dY_id Y_id.
+ * fa_varlen_bwd is the product; fa_varlen_fwd produces the Y and softmax
+ * statistics it consumes.
+ *
+ * Layout (parameter table + constraint section of that page).
+ *   q, dy, y, dq : [total_q,  head_num,    head_dim], contiguous, row-major
+ *   k, v, dk, dv : [total_kv, head_num_kv, head_dim], contiguous
+ *   Sequence b owns rows [sum_{b'<b} L_b', sum_{b'<=b} L_b') of T ("T is B and
+ *   S merged, packed tightly").  Element (t, n, d) sits at (t*N + n)*D + d.
+ *   softmax_max, softmax_sum : float32 [total_q, head_num, 8] (the
+ *   constraint section's TND statistics shape); lane 0 is read, the forward
+ *   writes all 8 lanes.  max = row maximum of the scaled, masked logits;
+ *   sum = sum_j exp(S_ij - max).  A row with no allowed key: max = -inf,
+ *   sum = 0.
+ *   seq_lens_q / seq_lens_kv : HOST arrays of `batch` int64 per-sequence
+ *   actual lengths (actualSeqQLen / actualSeqKvLen), zero allowed.
+ *   drop_mask : optional device bit mask, one bit per (b, n, i, j) at index
+ *   O_b + (n*Lq_b + i)*Lk_b + j with O_b = N * sum_{b'<b} Lq_b'*Lk_b',
+ *   least significant bit first, 1 = keep.  Read only when keep_prob < 1.
+ *   Mask: key j is allowed for query i (0-based inside the sequence) iff
+ *   i - pre_tokens <= j <= i + next_tokens (preTokens / nextTokens rows of
+ *   the parameter table).  Causal = next_tokens 0, pre_tokens >= max length.
+ *   Grouped heads: query head n uses key/value head n / (head_num/head_num_kv)
+ *   (constraint section: Nq/Nkv must be an integer).
+ *
+ * Ownership.  The caller owns every buffer, including the workspace, which
+ * is sized by the *_workspace_size call first (the page's two-phase
+ * GetWorkspaceSize / execute interface).  The library keeps no state
+ * between calls except per-device kernel attributes.
+ *
+ * Asynchrony.  Compute calls only enqueue work on `stream` and return; the
+ * only host-visible effects before the stream completes are argument
+ * checks.  Schedules derived from the host length arrays are copied into
+ * the workspace with one cudaMemcpyAsync per call.
+ *
+ * Errors (the page's return-code table: ACLNN_ERR_PARAM_NULLPTR for a null
+ * required pointer, ACLNN_ERR_PARAM_INVALID for out-of-range arguments):
+ *   FA_ERR_NULLPTR     a required pointer is NULL
+ *   FA_ERR_INVALID     layout != "TND", head_num not in [1, 256], head_dim
+ *                      not in [1, 768], keep_prob not in (0, 1], batch not
+ *                      in [1, 2048], a negative length, lengths not summing
+ *                      to total_q / total_kv, total_q > 1M, head_num not a
+ *                      multiple of head_num_kv, unknown dtype, non-finite
+ *                      scale, drop_mask_bytes too small
+ *   FA_ERR_UNSUPPORTED a valid request this build does not implement:
+ *                      head_dim not in {64, 128}, sparse_mode != 0
+ *   FA_ERR_WORKSPACE   workspace_bytes below the size the size call gave
+ *   FA_ERR_CUDA        a CUDA launch or copy failed
+ *   FA_ERR_TIMEOUT     (fa_varlen_read_error only) a kernel's bounded wait
+ *                      expired; its outputs are invalid
+ * Empty input: total_q == total_kv == 0 returns FA_OK without launching
+ * anything; with total_q == 0 alone the backward writes zero dk / dv.
+ */
+#ifndef FA_VARLEN_H
+#define FA_VARLEN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (NULL = the legacy default stream). */
+typedef struct CUstream_st *fa_stream_t;
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_NULLPTR = 1,
+  FA_ERR_INVALID = 2,
+  FA_ERR_UNSUPPORTED = 3,
+  FA_ERR_WORKSPACE = 4,
+  FA_ERR_CUDA = 5,
+  FA_ERR_TIMEOUT = 6
+} fa_status;
+
+/* Storage type of q, k, v, dy, y, dq, dk, dv (parameter table: FLOAT16,
+ * BFLOAT16, FLOAT32; all of them share one type). */
+typedef enum { FA_DTYPE_FP32 = 0, FA_DTYPE_FP16 = 1, FA_DTYPE_BF16 = 2 } fa_dtype;
+
+/* Backward kernel choice (fa_varlen_bwd_ex).  AUTO picks the tcgen05
+ * tensor-core kernel for 16-bit types and the fp32 CUDA-core kernel for
+ * FLOAT32; SIMT forces the CUDA-core kernel for any type. */
+typedef enum { FA_BWD_AUTO = 0, FA_BWD_SIMT = 1, FA_BWD_TCGEN05 = 2 } fa_bwd_impl;
+
+typedef struct {
+  int32_t impl;            /* fa_bwd_impl */
+  int32_t deterministic;   /* reserved, must be 0 */
+  int64_t wait_timeout_ns; /* bound on every in-kernel wait; <= 0: 2 s */
+  /* Optional cudaEvent_t[4] (caller-created, may be NULL): recorded on
+   * `stream` before the preprocess kernel, before the main kernel, after the
+   * main kernel and after the dQ convert kernel, for per-kernel timing. */
+  void *const *events;
+} fa_bwd_options;
+
+/* Forward workspace size in bytes (same scalar arguments as fa_varlen_fwd). */
+fa_status fa_varlen_fwd_workspace_size(
+    const int64_t *seq_lens_q, const int64_t *seq_lens_kv, int64_t batch,
+    int64_t total_q, int64_t total_kv, int64_t head_num, int64_t head_num_kv,
+    int64_t head_dim, fa_dtype dtype, const char *layout, double keep_prob,
+    int64_t pre_tokens, int64_t next_tokens, int64_t sparse_mode,
+    size_t *workspace_bytes);
+
+/* Forward: y (attentionIn of the backward) and the [T, N, 8] statistics. */
+fa_status fa_varlen_fwd(
+    const void *q, const void *k, const void *v,
+    const uint8_t *drop_mask, int64_t drop_mask_bytes,
+    const int64_t *seq_lens_q, const int64_t *seq_lens_kv, int64_t batch,
+    int64_t total_q, int64_t total_kv, int64_t head_num, int64_t head_num_kv,
+    int64_t head_dim, fa_dtype dtype, const char *layout, double scale,
+    double keep_prob, int64_t pre_tokens, int64_t next_tokens,
+    int64_t sparse_mode,
+    void *y, float *softmax_max, float *softmax_sum,
+    void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/* Backward workspace size in bytes.  Depends on the lengths, head counts,
+ * head_dim and the kernel AUTO would choose for `dtype`. */
+fa_status fa_varlen_bwd_workspace_size(
+    const int64_t *seq_lens_q, const int64_t *seq_lens_kv, int64_t batch,
+    int64_t total_q, int64_t total_kv, int64_t head_num, int64_t head_num_kv,
+    int64_t head_dim, fa_dtype dtype, const char *layout, double keep_prob,
+    int64_t pre_tokens, int64_t next_tokens, int64_t sparse_mode,
+    size_t *workspace_bytes);
+
+/* Backward: dq, dk, dv from q, k, v, dy, y (attentionIn) and the forward
+ * statistics.  dq, dk, dv are fully overwritten (rows of keys that no query
+ * attends to get zeros).  Non-deterministic: dq is summed with fp32 atomics
+ * (the constraint section: non-deterministic by default). */
+fa_status fa_varlen_bwd(
+    const void *q, const void *k, const void *v, const void *dy,
+    const uint8_t *drop_mask, int64_t drop_mask_bytes,
+    const float *softmax_max, const float *softmax_sum, const void *y,
+    const int64_t *seq_lens_q, const int64_t *seq_lens_kv, int64_t batch,
+    int64_t total_q, int64_t total_kv, int64_t head_num, int64_t head_num_kv,
+    int64_t head_dim, fa_dtype dtype, const char *layout, double scale,
+    double keep_prob, int64_t pre_tokens, int64_t next_tokens,
+    int64_t sparse_mode,
+    void *dq, void *dk, void *dv,
+    void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/* fa_varlen_bwd with options (NULL = defaults).  Its workspace is sized by
+ * fa_varlen_bwd_workspace_size_ex with the same options. */
+fa_status fa_varlen_bwd_workspace_size_ex(
+    const int64_t *seq_lens_q, const int64_t *seq_lens_kv, int64_t batch,
+    int64_t total_q, int64_t total_kv, int64_t head_num, int64_t head_num_kv,
+    int64_t head_dim, fa_dtype dtype, const char *layout, double keep_prob,
+    int64_t pre_tokens, int64_t next_tokens, int64_t sparse_mode,
+    const fa_bwd_options *options, size_t *workspace_bytes);
+
+fa_status fa_varlen_bwd_ex(
+    const void *q, const void *k, const void *v, const void *dy,
+    const uint8_t *drop_mask, int64_t drop_mask_bytes,
+    const float *softmax_max, const float *softmax_sum, const void *y,
+    const int64_t *seq_lens_q, const int64_t *seq_lens_kv, int64_t batch,
+    int64_t total_q, int64_t total_kv, int64_t head_num, int64_t head_num_kv,
+    int64_t head_dim, fa_dtype dtype, const char *layout, double scale,
+    double keep_prob, int64_t pre_tokens, int64_t next_tokens,
+    int64_t sparse_mode,
+    void *dq, void *dk, void *dv,
+    void *workspace, size_t workspace_bytes, fa_stream_t stream,
+    const fa_bwd_options *options);
+
+/* Reads the error word that the last call on `workspace` left in it, after
+ * synchronising `stream`: FA_OK, or FA_ERR_TIMEOUT when a bounded in-kernel
+ * wait expired.  *code receives the raw word (0 = no error). */
+fa_status fa_varlen_read_error(const void *workspace, size_t workspace_bytes,
+                               fa_stream_t stream, int32_t *code);
+
+/* Human-readable name of a status. */
+const char *fa_status_string(fa_status status);
+
+/* Synthetic-input utility (no part of the attention arithmetic): fills
+ * mask[0, ceil(nbits/8)) with SplitMix64 keep bits, bit g = 1 iff
+ * splitmix64(seed, g) < floor(keep_prob * 2^64), LSB first; bits past nbits
+ * in the last byte are 0.  Asynchronous on `stream`. */
+fa_status fa_gen_keep_mask(uint8_t *mask, int64_t nbits, uint64_t seed,
+                           double keep_prob, fa_stream_t stream);
+
+/* Host-only introspection of the backward tile scheduler (no GPU needed).
+ * Writes the work list the backward would run, in launch order, as 4 int32
+ * per item: {sequence, key/value head, key tile, lo | count << 16}, meaning
+ * key rows [tile*kv_tile, tile*kv_tile + kv_tile) of that sequence and head
+ * visit query tiles of 64 rows [lo, lo + count) of every query head of the
+ * group.  kv_tile is 64 (CUDA-core kernel) or 128 (tcgen05 kernel).
+ * *n_items receives the item count; at most `capacity` items are written.
+ * Errors: FA_ERR_NULLPTR, FA_ERR_INVALID (batch, lengths, head count,
+ * kv_tile out of range). */
+fa_status fa_varlen_bwd_schedule(const int64_t *seq_lens_q, const int64_t *seq_lens_kv,
+                                 int64_t batch, int64_t head_num_kv, int64_t pre_tokens,
+                                 int64_t next_tokens, int32_t kv_tile, int32_t *items,
+                                 int64_t capacity, int64_t *n_items);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t fa_varlen_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_VARLEN_H */

@@ -1,0 +1,501 @@
+// Host side of the C ABI: argument checks, the tile scheduler, the workspace
+// layout and the kernel launch sequence.
+//
+// The argument rules follow the FAG-V2 page (aclnnFlashAttentionUnpaddingScoreGradV2):
+// its return-code table (null required pointer -> ACLNN_ERR_PARAM_NULLPTR;
+// out-of-range type/format -> ACLNN_ERR_PARAM_INVALID), its constraint
+// section (TND only; T in [1, 1M]; N in [1, 256]; D in [1, 768]; keepProb in
+// (0, 1]; Nq/Nkv integer; at most 2K sequences; zero-length sequences
+// allowed) and its two-phase GetWorkspaceSize / execute interface.
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <vector>
+
+#include "internal.h"
+
+namespace fav {
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr size_t kHeaderBytes = 256;
+constexpr int64_t kMaxTotal = int64_t(1) << 20;   // T: 1 ~ 1M
+constexpr long long kDefaultTimeoutNs = 2000000000LL;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int clamp_window(int64_t x) {
+  const int64_t lim = int64_t(1) << 30;
+  return int(std::max(-lim, std::min(lim, x)));
+}
+
+struct Problem {
+  const int64_t *lens_q, *lens_kv;
+  int64_t batch, total_q, total_kv, n, n_kv, d;
+  fa_dtype dtype;
+  double keep_prob;
+  int64_t pre, next, sparse_mode;
+  int64_t tp;         // padded statistics rows
+  int64_t mask_bits;
+};
+
+// Checks shared by every entry point.  `need_ptrs` lists pointers that must
+// be non-null.
+fa_status check_problem(Problem &pr, const char *layout,
+                        std::initializer_list<const void *> need_ptrs) {
+  for (const void *ptr : need_ptrs)
+    if (ptr == nullptr) return FA_ERR_NULLPTR;
+  if (pr.lens_q == nullptr || pr.lens_kv == nullptr || layout == nullptr) return FA_ERR_NULLPTR;
+  if (std::strcmp(layout, "TND") != 0) return FA_ERR_INVALID;
+  if (pr.dtype != FA_DTYPE_FP32 && pr.dtype != FA_DTYPE_FP16 && pr.dtype != FA_DTYPE_BF16)
+    return FA_ERR_INVALID;
+  if (pr.n < 1 || pr.n > 256) return FA_ERR_INVALID;
+  if (pr.n_kv < 1 || pr.n_kv > pr.n || pr.n % pr.n_kv != 0) return FA_ERR_INVALID;
+  if (pr.d < 1 || pr.d > 768) return FA_ERR_INVALID;
+  if (!(pr.keep_prob > 0.0 && pr.keep_prob <= 1.0)) return FA_ERR_INVALID;
+  if (pr.batch < 1 || pr.batch > kMaxBatch) return FA_ERR_INVALID;
+  if (pr.total_q < 0 || pr.total_q > kMaxTotal || pr.total_kv < 0 || pr.total_kv > kMaxTotal)
+    return FA_ERR_INVALID;
+  int64_t sq = 0, sk = 0, tp = 0, bits = 0;
+  for (int64_t b = 0; b < pr.batch; ++b) {
+    const int64_t lq = pr.lens_q[b], lk = pr.lens_kv[b];
+    if (lq < 0 || lk < 0) return FA_ERR_INVALID;
+    sq += lq;
+    sk += lk;
+    tp += ceil_div(lq, kQTile) * kQTile;
+    bits += pr.n * lq * lk;
+  }
+  if (sq != pr.total_q || sk != pr.total_kv) return FA_ERR_INVALID;
+  if (pr.sparse_mode != 0) return FA_ERR_UNSUPPORTED;
+  if (pr.d != 64 && pr.d != 128) return FA_ERR_UNSUPPORTED;
+  pr.tp = tp;
+  pr.mask_bits = bits;
+  return FA_OK;
+}
+
+std::vector<SeqInfo> build_seqs(const Problem &pr) {
+  std::vector<SeqInfo> s(size_t(pr.batch));
+  int64_t cq = 0, ck = 0, qp = 0, mo = 0;
+  for (int64_t b = 0; b < pr.batch; ++b) {
+    const int64_t lq = pr.lens_q[b], lk = pr.lens_kv[b];
+    s[b].cu_q = int32_t(cq);
+    s[b].cu_k = int32_t(ck);
+    s[b].len_q = int32_t(lq);
+    s[b].len_k = int32_t(lk);
+    s[b].qpad = int32_t(qp);
+    s[b].pad_ = 0;
+    s[b].mask_off = mo;
+    cq += lq;
+    ck += lk;
+    qp += ceil_div(lq, kQTile) * kQTile;
+    mo += pr.n * lq * lk;
+  }
+  return s;
+}
+
+// Backward work list: one item per (sequence, key/value head, key tile).  A
+// key tile [k0, k1) sees queries i with k0 - next <= i <= k1 - 1 + pre; only
+// the query tiles meeting that range are visited, so fully masked causal or
+// band tiles cost nothing.  Items are ordered longest first (LPT) so the
+// tail of the grid holds the short ones.
+std::vector<WorkItem> build_bwd_items(const Problem &pr, int kv_tile) {
+  std::vector<WorkItem> items;
+  for (int64_t b = 0; b < pr.batch; ++b) {
+    const int64_t lq = pr.lens_q[b], lk = pr.lens_kv[b];
+    const int64_t tiles = ceil_div(lk, kv_tile);
+    for (int64_t t = 0; t < tiles; ++t) {
+      const int64_t k0 = t * kv_tile, k1 = std::min(lk, k0 + kv_tile);
+      const int64_t lo = std::max<int64_t>(0, k0 - pr.next);
+      const int64_t hi = std::min<int64_t>(lq - 1, k1 - 1 + pr.pre);
+      int64_t qlo = 0, cnt = 0;
+      if (lq > 0 && lo <= hi) {
+        qlo = lo / kQTile;
+        cnt = hi / kQTile - qlo + 1;
+      }
+      for (int64_t h = 0; h < pr.n_kv; ++h)
+        items.push_back({int32_t(b), int32_t(h), int32_t(t), int32_t(qlo | (cnt << 16))});
+    }
+  }
+  std::stable_sort(items.begin(), items.end(), [](const WorkItem &a, const WorkItem &c) {
+    return item_count(a) > item_count(c);
+  });
+  return items;
+}
+
+// Forward work list: one item per (sequence, query head, query tile) with the
+// key tiles its window meets.
+std::vector<WorkItem> build_fwd_items(const Problem &pr) {
+  std::vector<WorkItem> items;
+  for (int64_t b = 0; b < pr.batch; ++b) {
+    const int64_t lq = pr.lens_q[b], lk = pr.lens_kv[b];
+    const int64_t tiles = ceil_div(lq, kQTile);
+    for (int64_t t = 0; t < tiles; ++t) {
+      const int64_t q0 = t * kQTile, q1 = std::min(lq, q0 + kQTile);
+      const int64_t lo = std::max<int64_t>(0, q0 - pr.pre);
+      const int64_t hi = std::min<int64_t>(lk - 1, q1 - 1 + pr.next);
+      int64_t klo = 0, cnt = 0;
+      if (lk > 0 && lo <= hi) {
+        klo = lo / kSimtKvTile;
+        cnt = hi / kSimtKvTile - klo + 1;
+      }
+      for (int64_t h = 0; h < pr.n; ++h)
+        items.push_back({int32_t(b), int32_t(h), int32_t(t), int32_t(klo | (cnt << 16))});
+    }
+  }
+  std::stable_sort(items.begin(), items.end(), [](const WorkItem &a, const WorkItem &c) {
+    return item_count(a) > item_count(c);
+  });
+  return items;
+}
+
+int64_t count_items(const Problem &pr, int tile, bool fwd) {
+  int64_t c = 0;
+  for (int64_t b = 0; b < pr.batch; ++b)
+    c += fwd ? ceil_div(pr.lens_q[b], tile) * pr.n : ceil_div(pr.lens_kv[b], tile) * pr.n_kv;
+  return c;
+}
+
+struct BwdLayout {
+  size_t seqs, items, lse, dsum, dqacc, total;
+};
+
+int choose_bwd_impl(const Problem &pr, const fa_bwd_options *opt) {
+  int impl = opt ? opt->impl : FA_BWD_AUTO;
+  if (impl == FA_BWD_AUTO)
+    impl = tcgen05_supported(pr.dtype, int(pr.d)) ? FA_BWD_TCGEN05 : FA_BWD_SIMT;
+  return impl;
+}
+
+BwdLayout bwd_layout(const Problem &pr, int impl) {
+  // The item area is sized for the finer 64-key tiling so that a workspace
+  // sized for one kernel also fits the other (see choose_bwd_impl's fallback).
+  (void)impl;
+  const int tile = kSimtKvTile;
+  BwdLayout L;
+  size_t off = kHeaderBytes;
+  L.seqs = off;
+  off = align_up(off + sizeof(SeqInfo) * size_t(pr.batch));
+  L.items = off;
+  off = align_up(off + sizeof(WorkItem) * size_t(count_items(pr, tile, false)));
+  L.lse = off;
+  off = align_up(off + sizeof(float) * size_t(pr.n * pr.tp));
+  L.dsum = off;
+  off = align_up(off + sizeof(float) * size_t(pr.n * pr.tp));
+  L.dqacc = off;
+  off = align_up(off + sizeof(float) * size_t(pr.total_q * pr.n * pr.d));
+  L.total = off;
+  return L;
+}
+
+size_t fwd_layout_total(const Problem &pr, size_t *seqs_off, size_t *items_off) {
+  size_t off = kHeaderBytes;
+  *seqs_off = off;
+  off = align_up(off + sizeof(SeqInfo) * size_t(pr.batch));
+  *items_off = off;
+  off = align_up(off + sizeof(WorkItem) * size_t(count_items(pr, kQTile, true)));
+  return off;
+}
+
+// Uploads [header | seqs | items] with one copy; the header's error word is 0.
+fa_status upload_plan(void *ws, size_t seqs_off, size_t items_off,
+                      const std::vector<SeqInfo> &seqs, const std::vector<WorkItem> &items,
+                      cudaStream_t st) {
+  const size_t bytes = items_off + sizeof(WorkItem) * items.size();
+  std::vector<uint8_t> host(bytes, 0);
+  std::memcpy(host.data() + seqs_off, seqs.data(), sizeof(SeqInfo) * seqs.size());
+  if (!items.empty())
+    std::memcpy(host.data() + items_off, items.data(), sizeof(WorkItem) * items.size());
+  if (cudaMemcpyAsync(ws, host.data(), bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+uint64_t keep_threshold(double keep_prob, int *keep_all) {
+  *keep_all = keep_prob >= 1.0;
+  if (*keep_all) return ~uint64_t(0);
+  return uint64_t(keep_prob * 18446744073709551616.0);
+}
+
+}  // namespace
+}  // namespace fav
+
+using namespace fav;
+
+extern "C" {
+
+int32_t fa_varlen_version(void) { return 100; }
+
+const char *fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_NULLPTR: return "FA_ERR_NULLPTR: a required pointer is null";
+    case FA_ERR_INVALID: return "FA_ERR_INVALID: an argument is out of range";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: valid request not implemented by this build";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace too small";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call failed";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a bounded in-kernel wait expired";
+  }
+  return "unknown fa_status";
+}
+
+fa_status fa_varlen_fwd_workspace_size(const int64_t *seq_lens_q, const int64_t *seq_lens_kv,
+                                       int64_t batch, int64_t total_q, int64_t total_kv,
+                                       int64_t head_num, int64_t head_num_kv, int64_t head_dim,
+                                       fa_dtype dtype, const char *layout, double keep_prob,
+                                       int64_t pre_tokens, int64_t next_tokens,
+                                       int64_t sparse_mode, size_t *workspace_bytes) {
+  if (workspace_bytes == nullptr) return FA_ERR_NULLPTR;
+  Problem pr{seq_lens_q, seq_lens_kv, batch, total_q, total_kv, head_num, head_num_kv,
+             head_dim, dtype, keep_prob, pre_tokens, next_tokens, sparse_mode, 0, 0};
+  fa_status st = check_problem(pr, layout, {});
+  if (st != FA_OK) return st;
+  size_t a, b;
+  *workspace_bytes = fwd_layout_total(pr, &a, &b);
+  return FA_OK;
+}
+
+fa_status fa_varlen_fwd(const void *q, const void *k, const void *v, const uint8_t *drop_mask,
+                        int64_t drop_mask_bytes, const int64_t *seq_lens_q,
+                        const int64_t *seq_lens_kv, int64_t batch, int64_t total_q,
+                        int64_t total_kv, int64_t head_num, int64_t head_num_kv,
+                        int64_t head_dim, fa_dtype dtype, const char *layout, double scale,
+                        double keep_prob, int64_t pre_tokens, int64_t next_tokens,
+                        int64_t sparse_mode, void *y, float *softmax_max, float *softmax_sum,
+                        void *workspace, size_t workspace_bytes, fa_stream_t stream) {
+  Problem pr{seq_lens_q, seq_lens_kv, batch, total_q, total_kv, head_num, head_num_kv,
+             head_dim, dtype, keep_prob, pre_tokens, next_tokens, sparse_mode, 0, 0};
+  // Pointers of an empty side (no query rows / no key rows) may be null.
+  const bool hq = total_q > 0, hk = total_kv > 0;
+  const void *ok = &pr;
+  auto req = [ok](bool need, const void *ptr) { return need ? ptr : ok; };
+  fa_status st = check_problem(pr, layout,
+                               {req(hq, q), req(hk, k), req(hk, v), req(hq, y),
+                                req(hq, softmax_max), req(hq, softmax_sum)});
+  if (st != FA_OK) return st;
+  const bool dropout = keep_prob < 1.0;
+  if (dropout && drop_mask == nullptr) return FA_ERR_NULLPTR;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID;
+  if (dropout && drop_mask_bytes < (pr.mask_bits + 7) / 8) return FA_ERR_INVALID;
+  if (total_q == 0) return FA_OK;
+  size_t seqs_off, items_off;
+  const size_t need = fwd_layout_total(pr, &seqs_off, &items_off);
+  if (workspace == nullptr) return FA_ERR_NULLPTR;
+  if (workspace_bytes < need) return FA_ERR_WORKSPACE;
+
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  auto seqs = build_seqs(pr);
+  auto items = build_fwd_items(pr);
+  st = upload_plan(workspace, seqs_off, items_off, seqs, items, cs);
+  if (st != FA_OK) return st;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  FwdParams p{};
+  p.q = q; p.k = k; p.v = v;
+  p.mask = drop_mask; p.mask_bytes = drop_mask_bytes;
+  p.y = y; p.smax = softmax_max; p.ssum = softmax_sum;
+  p.seqs = reinterpret_cast<const SeqInfo *>(ws + seqs_off);
+  p.items = reinterpret_cast<const WorkItem *>(ws + items_off);
+  p.n_items = int(items.size());
+  p.batch = int(batch); p.n = int(head_num); p.n_kv = int(head_num_kv); p.d = int(head_dim);
+  p.pre = clamp_window(pre_tokens); p.next = clamp_window(next_tokens);
+  p.scale = float(scale);
+  p.inv_keep = float(1.0 / keep_prob);
+  p.use_dropout = dropout;
+  if (launch_fwd_simt(p, dtype, cs) != cudaSuccess) return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+fa_status fa_varlen_bwd_workspace_size_ex(const int64_t *seq_lens_q, const int64_t *seq_lens_kv,
+                                          int64_t batch, int64_t total_q, int64_t total_kv,
+                                          int64_t head_num, int64_t head_num_kv,
+                                          int64_t head_dim, fa_dtype dtype, const char *layout,
+                                          double keep_prob, int64_t pre_tokens,
+                                          int64_t next_tokens, int64_t sparse_mode,
+                                          const fa_bwd_options *options,
+                                          size_t *workspace_bytes) {
+  if (workspace_bytes == nullptr) return FA_ERR_NULLPTR;
+  Problem pr{seq_lens_q, seq_lens_kv, batch, total_q, total_kv, head_num, head_num_kv,
+             head_dim, dtype, keep_prob, pre_tokens, next_tokens, sparse_mode, 0, 0};
+  fa_status st = check_problem(pr, layout, {});
+  if (st != FA_OK) return st;
+  if (options && (options->deterministic != 0 || options->impl < FA_BWD_AUTO ||
+                  options->impl > FA_BWD_TCGEN05))
+    return FA_ERR_INVALID;
+  const int impl = choose_bwd_impl(pr, options);
+  if (impl == FA_BWD_TCGEN05 && !tcgen05_supported(dtype, int(head_dim)))
+    return FA_ERR_UNSUPPORTED;
+  *workspace_bytes = bwd_layout(pr, impl).total;
+  return FA_OK;
+}
+
+fa_status fa_varlen_bwd_workspace_size(const int64_t *seq_lens_q, const int64_t *seq_lens_kv,
+                                       int64_t batch, int64_t total_q, int64_t total_kv,
+                                       int64_t head_num, int64_t head_num_kv, int64_t head_dim,
+                                       fa_dtype dtype, const char *layout, double keep_prob,
+                                       int64_t pre_tokens, int64_t next_tokens,
+                                       int64_t sparse_mode, size_t *workspace_bytes) {
+  return fa_varlen_bwd_workspace_size_ex(seq_lens_q, seq_lens_kv, batch, total_q, total_kv,
+                                         head_num, head_num_kv, head_dim, dtype, layout,
+                                         keep_prob, pre_tokens, next_tokens, sparse_mode,
+                                         nullptr, workspace_bytes);
+}
+
+fa_status fa_varlen_bwd_ex(const void *q, const void *k, const void *v, const void *dy,
+                           const uint8_t *drop_mask, int64_t drop_mask_bytes,
+                           const float *softmax_max, const float *softmax_sum, const void *y,
+                           const int64_t *seq_lens_q, const int64_t *seq_lens_kv,
+                           int64_t batch, int64_t total_q, int64_t total_kv, int64_t head_num,
+                           int64_t head_num_kv, int64_t head_dim, fa_dtype dtype,
+                           const char *layout, double scale, double keep_prob,
+                           int64_t pre_tokens, int64_t next_tokens, int64_t sparse_mode,
+                           void *dq, void *dk, void *dv, void *workspace,
+                           size_t workspace_bytes, fa_stream_t stream,
+                           const fa_bwd_options *options) {
+  Problem pr{seq_lens_q, seq_lens_kv, batch, total_q, total_kv, head_num, head_num_kv,
+             head_dim, dtype, keep_prob, pre_tokens, next_tokens, sparse_mode, 0, 0};
+  // Pointers of an empty side (no query rows / no key rows) may be null.
+  const bool hq = total_q > 0, hk = total_kv > 0;
+  const void *ok = &pr;
+  auto req = [ok](bool need, const void *ptr) { return need ? ptr : ok; };
+  fa_status st = check_problem(
+      pr, layout,
+      {req(hq, q), req(hk, k), req(hk, v), req(hq, dy), req(hq, softmax_max),
+       req(hq, softmax_sum), req(hq, y), req(hq, dq), req(hk, dk), req(hk, dv)});
+  if (st != FA_OK) return st;
+  const bool dropout = keep_prob < 1.0;
+  if (dropout && drop_mask == nullptr) return FA_ERR_NULLPTR;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID;
+  if (dropout && drop_mask_bytes < (pr.mask_bits + 7) / 8) return FA_ERR_INVALID;
+  if (options && (options->deterministic != 0 || options->impl < FA_BWD_AUTO ||
+                  options->impl > FA_BWD_TCGEN05))
+    return FA_ERR_INVALID;
+  int impl = choose_bwd_impl(pr, options);
+  if (impl == FA_BWD_TCGEN05 && !tcgen05_supported(dtype, int(head_dim)))
+    return FA_ERR_UNSUPPORTED;
+  if (total_q == 0 && total_kv == 0) return FA_OK;
+  // The tensor-core kernel reads q, k, v, dy through TMA, which needs 16-byte
+  // aligned bases; with no query rows there is nothing for it to do.
+  const auto al16 = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; };
+  const bool tma_ok = total_q > 0 && al16(q) && al16(k) && al16(v) && al16(dy);
+  if (impl == FA_BWD_TCGEN05 && !tma_ok) {
+    if (options && options->impl == FA_BWD_TCGEN05 && total_q > 0) return FA_ERR_UNSUPPORTED;
+    impl = FA_BWD_SIMT;
+  }
+  const BwdLayout L = bwd_layout(pr, impl);
+  if (workspace == nullptr) return FA_ERR_NULLPTR;
+  if (workspace_bytes < L.total) return FA_ERR_WORKSPACE;
+
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const int tile = impl == FA_BWD_TCGEN05 ? kTcKvTile : kSimtKvTile;
+  auto seqs = build_seqs(pr);
+  auto items = build_bwd_items(pr, tile);
+  st = upload_plan(workspace, L.seqs, L.items, seqs, items, cs);
+  if (st != FA_OK) return st;
+
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  BwdParams p{};
+  p.q = q; p.k = k; p.v = v; p.dy = dy; p.y = y;
+  p.smax = softmax_max; p.ssum = softmax_sum;
+  p.mask = drop_mask; p.mask_bytes = drop_mask_bytes;
+  p.dq = dq; p.dk = dk; p.dv = dv;
+  p.seqs = reinterpret_cast<const SeqInfo *>(ws + L.seqs);
+  p.items = reinterpret_cast<const WorkItem *>(ws + L.items);
+  p.lse2 = reinterpret_cast<float *>(ws + L.lse);
+  p.dsum = reinterpret_cast<float *>(ws + L.dsum);
+  p.dq_acc = reinterpret_cast<float *>(ws + L.dqacc);
+  p.err = reinterpret_cast<int32_t *>(ws);
+  p.n_items = int(items.size());
+  p.batch = int(batch); p.n = int(head_num); p.n_kv = int(head_num_kv); p.d = int(head_dim);
+  p.tp = int(pr.tp); p.total_q = int(total_q); p.total_kv = int(total_kv);
+  p.pre = clamp_window(pre_tokens); p.next = clamp_window(next_tokens);
+  p.scale = float(scale);
+  p.scale_log2 = float(scale * 1.4426950408889634);
+  p.inv_keep = float(1.0 / keep_prob);
+  p.use_dropout = dropout;
+  p.timeout_ns = (options && options->wait_timeout_ns > 0) ? options->wait_timeout_ns
+                                                           : kDefaultTimeoutNs;
+
+  void *const *ev = options ? options->events : nullptr;
+  auto mark = [&](int i) {
+    return ev == nullptr || ev[i] == nullptr ||
+           cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), cs) == cudaSuccess;
+  };
+  if (!mark(0)) return FA_ERR_CUDA;
+  if (pr.tp > 0 && launch_bwd_preprocess(p, dtype, cs) != cudaSuccess) return FA_ERR_CUDA;
+  if (!mark(1)) return FA_ERR_CUDA;
+  if (!items.empty()) {
+    cudaError_t e = impl == FA_BWD_TCGEN05 ? launch_bwd_tcgen05(p, dtype, cs)
+                                           : launch_bwd_simt(p, dtype, cs);
+    if (e != cudaSuccess) return FA_ERR_CUDA;
+  }
+  if (!mark(2)) return FA_ERR_CUDA;
+  if (total_q > 0 && launch_dq_convert(p, dtype, cs) != cudaSuccess) return FA_ERR_CUDA;
+  if (!mark(3)) return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+fa_status fa_varlen_bwd(const void *q, const void *k, const void *v, const void *dy,
+                        const uint8_t *drop_mask, int64_t drop_mask_bytes,
+                        const float *softmax_max, const float *softmax_sum, const void *y,
+                        const int64_t *seq_lens_q, const int64_t *seq_lens_kv, int64_t batch,
+                        int64_t total_q, int64_t total_kv, int64_t head_num,
+                        int64_t head_num_kv, int64_t head_dim, fa_dtype dtype,
+                        const char *layout, double scale, double keep_prob,
+                        int64_t pre_tokens, int64_t next_tokens, int64_t sparse_mode, void *dq,
+                        void *dk, void *dv, void *workspace, size_t workspace_bytes,
+                        fa_stream_t stream) {
+  return fa_varlen_bwd_ex(q, k, v, dy, drop_mask, drop_mask_bytes, softmax_max, softmax_sum,
+                          y, seq_lens_q, seq_lens_kv, batch, total_q, total_kv, head_num,
+                          head_num_kv, head_dim, dtype, layout, scale, keep_prob, pre_tokens,
+                          next_tokens, sparse_mode, dq, dk, dv, workspace, workspace_bytes,
+                          stream, nullptr);
+}
+
+fa_status fa_varlen_read_error(const void *workspace, size_t workspace_bytes, fa_stream_t stream,
+                               int32_t *code) {
+  if (workspace == nullptr || code == nullptr) return FA_ERR_NULLPTR;
+  if (workspace_bytes < sizeof(int32_t)) return FA_ERR_WORKSPACE;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  int32_t word = 0;
+  if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (cudaStreamSynchronize(cs) != cudaSuccess) return FA_ERR_CUDA;
+  *code = word;
+  return word == 0 ? FA_OK : FA_ERR_TIMEOUT;
+}
+
+fa_status fa_varlen_bwd_schedule(const int64_t *seq_lens_q, const int64_t *seq_lens_kv,
+                                 int64_t batch, int64_t head_num_kv, int64_t pre_tokens,
+                                 int64_t next_tokens, int32_t kv_tile, int32_t *items,
+                                 int64_t capacity, int64_t *n_items) {
+  if (seq_lens_q == nullptr || seq_lens_kv == nullptr || n_items == nullptr) return FA_ERR_NULLPTR;
+  if (capacity > 0 && items == nullptr) return FA_ERR_NULLPTR;
+  if (batch < 1 || batch > kMaxBatch || head_num_kv < 1 || head_num_kv > 256) return FA_ERR_INVALID;
+  if (kv_tile != kSimtKvTile && kv_tile != kTcKvTile) return FA_ERR_INVALID;
+  for (int64_t b = 0; b < batch; ++b)
+    if (seq_lens_q[b] < 0 || seq_lens_kv[b] < 0 || seq_lens_q[b] > (int64_t(1) << 20) ||
+        seq_lens_kv[b] > (int64_t(1) << 20))
+      return FA_ERR_INVALID;
+  Problem pr{seq_lens_q, seq_lens_kv, batch, 0, 0, head_num_kv, head_num_kv, 128,
+             FA_DTYPE_BF16, 1.0, pre_tokens, next_tokens, 0, 0, 0};
+  auto list = build_bwd_items(pr, kv_tile);
+  *n_items = int64_t(list.size());
+  const int64_t m = std::min<int64_t>(capacity, int64_t(list.size()));
+  if (m > 0) std::memcpy(items, list.data(), size_t(m) * sizeof(WorkItem));
+  return FA_OK;
+}
+
+fa_status fa_gen_keep_mask(uint8_t *mask, int64_t nbits, uint64_t seed, double keep_prob,
+                           fa_stream_t stream) {
+  if (mask == nullptr) return FA_ERR_NULLPTR;
+  if (nbits < 0 || !(keep_prob > 0.0 && keep_prob <= 1.0)) return FA_ERR_INVALID;
+  if (nbits == 0) return FA_OK;
+  int keep_all = 0;
+  const uint64_t thr = keep_threshold(keep_prob, &keep_all);
+  if (launch_gen_keep_mask(mask, nbits, seed, thr, keep_all,
+                           reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,562 @@
+// Backward of varlen attention on the sm_103a tensor cores (tcgen05 + TMEM +
+// TMA), head_dim 128, bf16 or fp16 storage.
+//
+// It computes the FAG-V2 page's backward (aclnnFlashAttentionUnpaddingScoreGradV2,
+// section 功能说明 / 计算公式: dV = P^T dY, dQ = dS K / sqrt(d),
+// dK = dS^T Q / sqrt(d), with scaleValue in place of 1/sqrt(d)), recomputing
+// P from the saved softmax statistics.
+//
+// One CTA per work item: 128 keys of one (sequence, key/value head), looping
+// over the 64-row query tiles the window reaches, for every query head of the
+// group.  Per query tile the five contractions run on the tensor core with
+// fp32 accumulators in TMEM (keys on the M side, so P^T and dS^T are already
+// in the A-operand layout):
+//
+//   S^T  = K Q^T          M=128 keys, N=64 queries, K=128 (A, B in smem, K-major)
+//   dP^T = V dY^T         same shape
+//   dV  += P^T dY         M=128 keys, N=128 d, K=64 (A = P^T in TMEM, B = dY MN-major)
+//   dK  += dS^T Q         same, A = dS^T in TMEM, B = Q
+//   dQ^T = K^T dS^T       M=128 d, N=64 queries, K=128 keys (A = K MN-major, B = dS^T)
+//
+// dQ^T is drained from TMEM and added into the fp32 dq_acc with coalesced
+// reductions (one 128-byte row segment per warp instruction); dK and dV stay
+// in TMEM for the whole item and are written once at the end.
+//
+// Warp roles (16 warps):
+//   0      TMA producer: K, V once; Q, dY, lse, D per query tile (2 stages)
+//   1      MMA issuer (one thread); the warp owns the TMEM allocation
+//   2-3    idle
+//   4-11   softmax: TMEM lane quarter = warp % 4 (one key per thread), column
+//          half = (warp - 4) / 4 (32 of the 64 queries); P, dropout, dS; then
+//          the dV (first half) / dK (second half) epilogue
+//   12-15  dQ drain: TMEM lane = d
+//
+// Every mbarrier wait is bounded (BwdParams::timeout_ns); a wait that gives up
+// records kErrTimeoutBase + role in the workspace error word, and the CTA
+// winds down without further waits except bounded ones for its own copies
+// and MMAs in flight, then frees TMEM.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include <mutex>
+#include <type_traits>
+
+#include "common.cuh"
+#include "sm103.cuh"
+
+namespace fav {
+namespace {
+
+using namespace sm103;
+
+constexpr int BN = kTcKvTile;   // 128 keys per item
+constexpr int BM = kQTile;      // 64 queries per iteration
+constexpr int HD = 128;         // head dim
+constexpr int STAGES = 2;
+constexpr int NTHREADS = 512;
+
+// TMEM columns (512 allocated; 128 lanes x 32-bit cells).
+constexpr uint32_t COL_DV = 0;     // 128: dV accumulator, lane = key
+constexpr uint32_t COL_DK = 128;   // 128: dK accumulator, lane = key
+constexpr uint32_t COL_S = 256;    //  64: S^T (fp32)
+constexpr uint32_t COL_DP = 320;   //  64: dP^T (fp32)
+constexpr uint32_t COL_DQ = 384;   //  64: dQ^T (fp32), lane = d
+constexpr uint32_t COL_P = 448;    //  32: P^T (bf16 pairs), MMA A operand
+constexpr uint32_t COL_DS = 480;   //  32: dS^T (bf16 pairs), MMA A operand
+
+// Shared memory (offsets from a 1024-byte aligned base).  Every tile is
+// stored as 64-column boxes of 128-byte rows in the TMA 128-byte swizzle.
+constexpr uint32_t SM_K = 0;                          // 2 boxes [128 x 64]
+constexpr uint32_t SM_V = SM_K + 32768;
+constexpr uint32_t SM_Q = SM_V + 32768;               // STAGES x 2 boxes [64 x 64]
+constexpr uint32_t SM_DY = SM_Q + STAGES * 16384;
+constexpr uint32_t SM_DS = SM_DY + STAGES * 16384;    // [128 keys x 64 queries]
+constexpr uint32_t SM_LSE = SM_DS + 16384;            // STAGES x 64 floats
+constexpr uint32_t SM_DSUM = SM_LSE + STAGES * 256;
+constexpr uint32_t SM_BAR = SM_DSUM + STAGES * 256;
+constexpr uint32_t SM_TOTAL = SM_BAR + 256;
+constexpr uint32_t SMEM_BYTES = SM_TOTAL + 1024;
+
+// mbarrier slots
+enum : int {
+  B_KV = 0, B_FULL = 1, B_EMPTY = B_FULL + STAGES, B_SFULL = B_EMPTY + STAGES, B_SFREE,
+  B_DPFULL, B_DPFREE, B_PFULL, B_PFREE, B_DSFULL, B_DSFREE, B_DQFULL, B_DQFREE, B_ACC,
+  B_FINAL, B_COUNT
+};
+static_assert(B_COUNT * 8 <= 256, "barrier area");
+
+enum : int { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_SOFTMAX = 3, ROLE_DQ = 4, ROLE_EPILOGUE = 5 };
+
+struct TcMaps {
+  CUtensorMap q, dy, k, v;
+};
+
+// Bits [bit, bit + 32) of the keep mask, read without leaving
+// [mask, mask + nbytes).
+__device__ __forceinline__ uint32_t fetch_bits32(const uint8_t *mask, int64_t nbytes,
+                                                 int64_t bit) {
+  const uintptr_t base = reinterpret_cast<uintptr_t>(mask);
+  const uintptr_t addr = base + uintptr_t(bit >> 3);
+  const uintptr_t al = addr & ~uintptr_t(3);
+  const int sh = int((addr - al) * 8 + uintptr_t(bit & 7));
+  const uintptr_t end = base + uintptr_t(nbytes);
+  uint32_t lo, hi;
+  if (al >= base && al + 8 <= end) {
+    lo = __ldg(reinterpret_cast<const uint32_t *>(al));
+    hi = __ldg(reinterpret_cast<const uint32_t *>(al + 4));
+  } else {
+    uint64_t w = 0;
+    for (int k = 0; k < 8; ++k) {
+      const uintptr_t a = al + k;
+      if (a >= base && a < end) w |= uint64_t(__ldg(reinterpret_cast<const uint8_t *>(a))) << (8 * k);
+    }
+    lo = uint32_t(w);
+    hi = uint32_t(w >> 32);
+  }
+  return __funnelshift_r(lo, hi, sh);
+}
+
+// 32 x 32 bit-matrix transpose across the warp: on return, bit c of lane j's
+// word is bit j of lane c's input word (recursive block swap).
+__device__ __forceinline__ uint32_t transpose_bits32(uint32_t w, int lane) {
+  const uint32_t masks[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+  for (int k = 0, s = 16; k < 5; ++k, s >>= 1) {
+    const uint32_t o = __shfl_xor_sync(0xffffffffu, w, s);
+    w = (lane & s) ? ((w & ~masks[k]) | ((o & ~masks[k]) >> s))
+                   : ((w & masks[k]) | ((o & masks[k]) << s));
+  }
+  return w;
+}
+
+template <bool kBF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  return kBF16 ? pack_bf16(lo, hi) : pack_f16(lo, hi);
+}
+
+__device__ __forceinline__ void red_add_f32(float *addr, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_global_v4(void *ptr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+struct Ctl {
+  int *abort;         // shared-memory flag: some wait of this CTA gave up
+  int32_t *err;       // global error word
+  long long timeout;
+};
+
+__device__ __forceinline__ bool wait_or_abort(const Ctl &c, uint32_t bar, uint32_t parity,
+                                              int role) {
+  if (mbar_wait(bar, parity, c.timeout, c.abort)) return true;
+  if (!*reinterpret_cast<volatile int *>(c.abort)) {
+    atomicExch(c.abort, 1);
+    atomicCAS(c.err, 0, kErrTimeoutBase + role);
+  }
+  return false;
+}
+
+template <bool kBF16>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    bwd_tc_kernel(const BwdParams p, const __grid_constant__ TcMaps maps) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                            ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  auto bar = [&](int i) { return sb + SM_BAR + 8u * uint32_t(i); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WorkItem item = p.items[blockIdx.x];
+  const SeqInfo sq = p.seqs[item.seq];
+  const int kvh = item.head;
+  const int group = p.n / p.n_kv;
+  const int k0 = item.tile * BN;
+  const int qlo = item_lo(item), qcnt = item_count(item);
+  const int n_it = qcnt * group;
+  Ctl ctl{&s_abort, p.err, p.timeout_ns};
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    mbar_init(bar(B_KV), 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar(B_FULL + s), 1);
+      mbar_init(bar(B_EMPTY + s), 1);
+    }
+    mbar_init(bar(B_SFULL), 1);
+    mbar_init(bar(B_SFREE), 8);
+    mbar_init(bar(B_DPFULL), 1);
+    mbar_init(bar(B_DPFREE), 8);
+    mbar_init(bar(B_PFULL), 8);
+    mbar_init(bar(B_PFREE), 1);
+    mbar_init(bar(B_DSFULL), 8);
+    mbar_init(bar(B_DSFREE), 1);
+    mbar_init(bar(B_DQFULL), 1);
+    mbar_init(bar(B_DQFREE), 4);
+    mbar_init(bar(B_ACC), 1);
+    mbar_init(bar(B_FINAL), 1);
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&s_tmem), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n_it > 0) {
+      tma_prefetch_map(&maps.q);
+      tma_prefetch_map(&maps.dy);
+      tma_prefetch_map(&maps.k);
+      tma_prefetch_map(&maps.v);
+      const int ky = sq.cu_k + k0, kx = kvh * HD;
+      mbar_arrive_expect_tx(bar(B_KV), 4 * 16384);
+      tma_load_2d(sb + SM_K, &maps.k, bar(B_KV), kx, ky);
+      tma_load_2d(sb + SM_K + 16384, &maps.k, bar(B_KV), kx + 64, ky);
+      tma_load_2d(sb + SM_V, &maps.v, bar(B_KV), kx, ky);
+      tma_load_2d(sb + SM_V + 16384, &maps.v, bar(B_KV), kx + 64, ky);
+      int issued = 0;
+      for (int L = 0; L < n_it; ++L) {
+        const int st = L % STAGES;
+        if (L >= STAGES && !wait_or_abort(ctl, bar(B_EMPTY + st), ((L / STAGES) - 1) & 1,
+                                          ROLE_PRODUCER))
+          break;
+        const int n = kvh * group + L / qcnt;
+        const int q0 = (qlo + L % qcnt) * BM;
+        const int qy = sq.cu_q + q0, qx = n * HD;
+        const uint32_t full = bar(B_FULL + st);
+        mbar_arrive_expect_tx(full, 4 * 8192 + 2 * 256);
+        tma_load_2d(sb + SM_Q + st * 16384, &maps.q, full, qx, qy);
+        tma_load_2d(sb + SM_Q + st * 16384 + 8192, &maps.q, full, qx + 64, qy);
+        tma_load_2d(sb + SM_DY + st * 16384, &maps.dy, full, qx, qy);
+        tma_load_2d(sb + SM_DY + st * 16384 + 8192, &maps.dy, full, qx + 64, qy);
+        const int64_t srow = int64_t(n) * p.tp + sq.qpad + q0;
+        bulk_load(sb + SM_LSE + st * 256, p.lse2 + srow, 256, full);
+        bulk_load(sb + SM_DSUM + st * 256, p.dsum + srow, 256, full);
+        ++issued;
+      }
+      // No copy may still be writing shared memory when the CTA exits.
+      const int never = 0;
+      mbar_wait(bar(B_KV), 0, p.timeout_ns, &never);
+      for (int L = issued > STAGES ? issued - STAGES : 0; L < issued; ++L)
+        mbar_wait(bar(B_FULL + L % STAGES), (L / STAGES) & 1, p.timeout_ns, &never);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_it > 0) {
+      const uint32_t id_s = idesc_f16(128, BM, false, false, kBF16);   // S^T, dP^T
+      const uint32_t id_g = idesc_f16(128, HD, false, true, kBF16);    // dV, dK
+      const uint32_t id_q = idesc_f16(128, BM, true, true, kBF16);     // dQ^T
+      auto mma_kt = [&](uint32_t a_base, uint32_t b_base, uint32_t dcol) {
+        // D[128 x 64] = A[128 x 128] B[64 x 128]^T, both K-major (2 boxes along K)
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk & 3) * 32;
+          const uint64_t a = sdesc_sw128(a_base + (kk >> 2) * 16384 + off, 16, 1024);
+          const uint64_t b = sdesc_sw128(b_base + (kk >> 2) * 8192 + off, 16, 1024);
+          mma_ss(tmem + dcol, a, b, id_s, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto mma_grad = [&](uint32_t a_col, uint32_t b_base, uint32_t dcol, bool acc) {
+        // D[128 x 128] += A[128 x 64] (TMEM) B[64 x 128] (MN-major)
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk) {
+          const uint64_t b = sdesc_sw128(b_base + kk * 2048, 8192, 1024);
+          mma_ts(tmem + dcol, tmem + a_col + kk * 8, b, id_g, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      auto mma_dq = [&]() {
+        // dQ^T[128 d x 64 q] = K^T[128 d x 128 keys] dS^T[128 keys x 64 q]
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t a = sdesc_sw128(sb + SM_K + kk * 2048, 16384, 1024);
+          const uint64_t b = sdesc_sw128(sb + SM_DS + kk * 2048, 16384, 1024);
+          mma_ss(tmem + COL_DQ, a, b, id_q, kk > 0 ? 1u : 0u);
+        }
+      };
+      bool ok = wait_or_abort(ctl, bar(B_KV), 0, ROLE_MMA) &&
+                wait_or_abort(ctl, bar(B_FULL), 0, ROLE_MMA);
+      tc_fence_after();
+      if (ok) {
+        mma_kt(sb + SM_K, sb + SM_Q, COL_S);
+        mma_commit(bar(B_SFULL));
+        mma_kt(sb + SM_V, sb + SM_DY, COL_DP);
+        mma_commit(bar(B_DPFULL));
+      }
+      for (int L = 0; ok && L < n_it; ++L) {
+        const int st = L % STAGES;
+        if (L + 1 < n_it) {
+          const int s1 = (L + 1) % STAGES;
+          ok = wait_or_abort(ctl, bar(B_FULL + s1), ((L + 1) / STAGES) & 1, ROLE_MMA) &&
+               wait_or_abort(ctl, bar(B_SFREE), L & 1, ROLE_MMA);
+          if (!ok) break;
+          tc_fence_after();
+          mma_kt(sb + SM_K, sb + SM_Q + s1 * 16384, COL_S);
+          mma_commit(bar(B_SFULL));
+        }
+        if (!(ok = wait_or_abort(ctl, bar(B_PFULL), L & 1, ROLE_MMA))) break;
+        tc_fence_after();
+        mma_grad(COL_P, sb + SM_DY + st * 16384, COL_DV, L > 0);
+        mma_commit(bar(B_PFREE));
+        if (!(ok = wait_or_abort(ctl, bar(B_DSFULL), L & 1, ROLE_MMA))) break;
+        tc_fence_after();
+        mma_grad(COL_DS, sb + SM_Q + st * 16384, COL_DK, L > 0);
+        if (L > 0 && !(ok = wait_or_abort(ctl, bar(B_DQFREE), (L - 1) & 1, ROLE_MMA))) break;
+        tc_fence_after();
+        mma_dq();
+        mma_commit(bar(B_DQFULL));
+        mma_commit(bar(B_DSFREE));
+        mma_commit(bar(B_EMPTY + st));
+        if (L + 1 < n_it) {
+          if (!(ok = wait_or_abort(ctl, bar(B_DPFREE), L & 1, ROLE_MMA))) break;
+          tc_fence_after();
+          mma_kt(sb + SM_V, sb + SM_DY + ((L + 1) % STAGES) * 16384, COL_DP);
+          mma_commit(bar(B_DPFULL));
+        }
+      }
+      if (ok) mma_commit(bar(B_ACC));
+      // Every MMA of this CTA has finished before TMEM is freed.
+      mma_commit(bar(B_FINAL));
+      const int never = 0;
+      mbar_wait(bar(B_FINAL), 0, p.timeout_ns, &never);
+    }
+  } else if (warp >= 4 && warp < 12) {
+    // ------------------------------------------------------------ softmax / dS
+    const int half = (warp - 4) >> 2;
+    const int quarter = warp & 3;
+    const int jl = quarter * 32 + lane;
+    const int jg = k0 + jl;
+    const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+    const float sl2 = p.scale_log2;
+    for (int L = 0; L < n_it; ++L) {
+      const int st = L % STAGES;
+      const int n = kvh * group + L / qcnt;
+      const int q0 = (qlo + L % qcnt) * BM;
+      const int i0 = q0 + 32 * half;
+      uint32_t r[32];
+      float pr[32];
+      if (!wait_or_abort(ctl, bar(B_SFULL), L & 1, ROLE_SOFTMAX)) break;
+      tc_fence_after();
+      tmem_ld32(tmem + lane_off + COL_S + 32 * half, r);
+      tc_fence_before();
+      if (lane == 0) mbar_arrive(bar(B_SFREE));
+      const float *lse = reinterpret_cast<const float *>(sm + SM_LSE + st * 256) + 32 * half;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) pr[c] = ex2(fmaf(__uint_as_float(r[c]), sl2, -lse[c]));
+      const bool full_tile = (k0 + BN - 1 <= q0 + p.next) && (k0 >= q0 + BM - 1 - p.pre) &&
+                             (k0 + BN <= sq.len_k);
+      if (!full_tile) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int i = i0 + c;
+          if (!(jg <= i + p.next && jg >= i - p.pre && jg < sq.len_k)) pr[c] = 0.f;
+        }
+      }
+      uint32_t keep = 0xFFFFFFFFu;
+      float zs = 1.f;
+      if (p.use_dropout) {
+        const int il = i0 + lane;
+        uint32_t w = 0;
+        if (il < sq.len_q) {
+          const int64_t bit = sq.mask_off + (int64_t(n) * sq.len_q + il) * sq.len_k + k0 +
+                              quarter * 32;
+          w = fetch_bits32(p.mask, p.mask_bytes, bit);
+        }
+        keep = transpose_bits32(w, lane);
+        zs = p.inv_keep;
+      }
+      uint32_t pk[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const float a = ((keep >> (2 * c)) & 1u) ? pr[2 * c] * zs : 0.f;
+        const float b = ((keep >> (2 * c + 1)) & 1u) ? pr[2 * c + 1] * zs : 0.f;
+        pk[c] = pack2<kBF16>(a, b);
+      }
+      if (L > 0 && !wait_or_abort(ctl, bar(B_PFREE), (L - 1) & 1, ROLE_SOFTMAX)) break;
+      tc_fence_after();
+      tmem_st16(tmem + lane_off + COL_P + 16 * half, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_PFULL));
+
+      if (!wait_or_abort(ctl, bar(B_DPFULL), L & 1, ROLE_SOFTMAX)) break;
+      tc_fence_after();
+      tmem_ld32(tmem + lane_off + COL_DP + 32 * half, r);
+      tc_fence_before();
+      if (lane == 0) mbar_arrive(bar(B_DPFREE));
+      const float *dsum = reinterpret_cast<const float *>(sm + SM_DSUM + st * 256) + 32 * half;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const float z0 = ((keep >> (2 * c)) & 1u) ? zs : 0.f;
+        const float z1 = ((keep >> (2 * c + 1)) & 1u) ? zs : 0.f;
+        const float d0 = pr[2 * c] * (__uint_as_float(r[2 * c]) * z0 - dsum[2 * c]);
+        const float d1 = pr[2 * c + 1] * (__uint_as_float(r[2 * c + 1]) * z1 - dsum[2 * c + 1]);
+        pk[c] = pack2<kBF16>(d0, d1);
+      }
+      if (L > 0 && !wait_or_abort(ctl, bar(B_DSFREE), (L - 1) & 1, ROLE_SOFTMAX)) break;
+      tc_fence_after();
+      tmem_st16(tmem + lane_off + COL_DS + 16 * half, pk);
+      const uint32_t row = sb + SM_DS + uint32_t(jl) * 128u;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const uint32_t chunk = uint32_t((4 * half + cc) ^ (jl & 7));
+        st_shared_v4(row + chunk * 16u, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_DSFULL));
+    }
+    // ------------------------------------------------------------ epilogue
+    bool have = n_it > 0 && !*reinterpret_cast<volatile int *>(&s_abort);
+    if (have) have = wait_or_abort(ctl, bar(B_ACC), 0, ROLE_EPILOGUE);
+    tc_fence_after();
+    if (n_it == 0 || have) {
+      using T = typename std::conditional<kBF16, __nv_bfloat16, __half>::type;
+      T *out = static_cast<T *>(half == 0 ? p.dv : p.dk);
+      const float sc = half == 0 ? 1.f : p.scale;
+      const uint32_t col = half == 0 ? COL_DV : COL_DK;
+      const bool valid = jg < sq.len_k;
+      T *rowp = out + ((int64_t(sq.cu_k) + jg) * p.n_kv + kvh) * HD;
+#pragma unroll 1
+      for (int c0 = 0; c0 < HD; c0 += 32) {
+        uint32_t r[32];
+        if (n_it > 0) {
+          tmem_ld32(tmem + lane_off + col + c0, r);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) r[c] = 0u;
+        }
+        if (valid) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[e] = pack2<kBF16>(__uint_as_float(r[8 * v + 2 * e]) * sc,
+                                  __uint_as_float(r[8 * v + 2 * e + 1]) * sc);
+            st_global_v4(rowp + c0 + 8 * v, w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+    }
+  } else if (warp >= 12) {
+    // ------------------------------------------------------------ dQ drain
+    const int quarter = warp & 3;
+    const int d = quarter * 32 + lane;
+    const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+    const int64_t row_stride = int64_t(p.n) * HD;
+    for (int L = 0; L < n_it; ++L) {
+      const int n = kvh * group + L / qcnt;
+      const int q0 = (qlo + L % qcnt) * BM;
+      if (!wait_or_abort(ctl, bar(B_DQFULL), L & 1, ROLE_DQ)) break;
+      tc_fence_after();
+      uint32_t a[32], b[32];
+      tmem_ld32(tmem + lane_off + COL_DQ, a);
+      tmem_ld32(tmem + lane_off + COL_DQ + 32, b);
+      tc_fence_before();
+      if (lane == 0) mbar_arrive(bar(B_DQFREE));
+      const int rows = min(BM, sq.len_q - q0);
+      float *base = p.dq_acc + (int64_t(sq.cu_q) + q0) * row_stride + int64_t(n) * HD + d;
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (c < rows) red_add_f32(base + c * row_stride, __uint_as_float(a[c]));
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (32 + c < rows) red_add_f32(base + (32 + c) * row_stride, __uint_as_float(b[c]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// [rows, heads * 128] 16-bit tensor as a 2-D map with 64-column x box_rows boxes.
+bool make_map(CUtensorMap *m, const void *base, int64_t rows, int heads, int box_rows, bool bf16) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {cuuint64_t(heads) * HD, cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(heads) * HD * 2};
+  cuuint32_t box[2] = {64, cuuint32_t(box_rows)};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+             const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool kBF16>
+cudaError_t launch_t(const BwdParams &p, cudaStream_t st) {
+  TcMaps maps;
+  if (!make_map(&maps.q, p.q, p.total_q, p.n, BM, kBF16) ||
+      !make_map(&maps.dy, p.dy, p.total_q, p.n, BM, kBF16) ||
+      !make_map(&maps.k, p.k, p.total_kv, p.n_kv, BN, kBF16) ||
+      !make_map(&maps.v, p.v, p.total_kv, p.n_kv, BN, kBF16))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<kBF16>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  bwd_tc_kernel<kBF16><<<p.n_items, NTHREADS, SMEM_BYTES, st>>>(p, maps);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tcgen05_supported(fa_dtype dt, int head_dim) {
+  return head_dim == HD && (dt == FA_DTYPE_BF16 || dt == FA_DTYPE_FP16);
+}
+
+cudaError_t launch_bwd_tcgen05(const BwdParams &p, fa_dtype dt, cudaStream_t s) {
+  if (dt == FA_DTYPE_BF16) return launch_t<true>(p, s);
+  if (dt == FA_DTYPE_FP16) return launch_t<false>(p, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fav

@@ -1,0 +1,90 @@
+// Internal declarations shared by the host side (abi.cpp) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fa_varlen.h"
+
+namespace fav {
+
+constexpr int kQTile = 64;        // query rows per tile, every kernel
+constexpr int kSimtKvTile = 64;   // key rows per work item, CUDA-core kernels
+constexpr int kTcKvTile = 128;    // key rows per work item, tcgen05 kernel
+constexpr int kMaxBatch = 2048;
+
+// One per sequence, uploaded into the workspace (32 bytes).
+struct SeqInfo {
+  int32_t cu_q;      // first row of the sequence in q / dy / y / dq
+  int32_t cu_k;      // first row in k / v / dk / dv
+  int32_t len_q;
+  int32_t len_k;
+  int32_t qpad;      // first row in the 64-row-padded statistics index space
+  int32_t pad_;
+  int64_t mask_off;  // dropout bit of (head 0, i 0, j 0): N * sum_{b'<b} Lq*Lk
+};
+
+// One unit of work.  Backward: key tile `tile` of sequence `seq` for key/value
+// head `head`, covering query tiles [lo, lo + count) of every query head of
+// the group.  Forward: query tile `tile` of query head `head`, covering key
+// tiles [lo, lo + count).
+struct WorkItem {
+  int32_t seq;
+  int32_t head;
+  int32_t tile;
+  int32_t range;     // lo | (count << 16)
+};
+
+__host__ __device__ inline int item_lo(const WorkItem &w) { return w.range & 0xFFFF; }
+__host__ __device__ inline int item_count(const WorkItem &w) { return (w.range >> 16) & 0xFFFF; }
+
+// Error word codes written by kernels into the workspace header.
+enum : int32_t {
+  kErrNone = 0,
+  kErrTimeoutBase = 0x100,   // + role id of the wait that expired
+};
+
+struct BwdParams {
+  const void *q, *k, *v, *dy, *y;
+  const float *smax, *ssum;
+  const uint8_t *mask;
+  int64_t mask_bytes;
+  void *dq, *dk, *dv;
+  const SeqInfo *seqs;
+  const WorkItem *items;
+  float *lse2;      // [N][Tp]  (max + ln sum) * log2(e); +inf for padding rows
+  float *dsum;      // [N][Tp]  sum_d dY * Y;               0 for padding rows
+  float *dq_acc;    // [Tq][N][D] fp32 accumulator of dS K (unscaled)
+  int32_t *err;
+  int n_items, batch, n, n_kv, d, tp, total_q, total_kv;
+  int pre, next;    // clamped to +-2^30
+  float scale, scale_log2, inv_keep;
+  int use_dropout;
+  long long timeout_ns;
+};
+
+struct FwdParams {
+  const void *q, *k, *v;
+  const uint8_t *mask;
+  int64_t mask_bytes;
+  void *y;
+  float *smax, *ssum;
+  const SeqInfo *seqs;
+  const WorkItem *items;
+  int n_items, batch, n, n_kv, d;
+  int pre, next;
+  float scale, inv_keep;
+  int use_dropout;
+};
+
+// Kernel launchers (return the launch error).
+cudaError_t launch_bwd_preprocess(const BwdParams &p, fa_dtype dt, cudaStream_t s);
+cudaError_t launch_bwd_simt(const BwdParams &p, fa_dtype dt, cudaStream_t s);
+cudaError_t launch_bwd_tcgen05(const BwdParams &p, fa_dtype dt, cudaStream_t s);
+cudaError_t launch_dq_convert(const BwdParams &p, fa_dtype dt, cudaStream_t s);
+cudaError_t launch_fwd_simt(const FwdParams &p, fa_dtype dt, cudaStream_t s);
+cudaError_t launch_gen_keep_mask(uint8_t *mask, int64_t nbits, uint64_t seed,
+                                 uint64_t threshold, int keep_all, cudaStream_t s);
+bool tcgen05_supported(fa_dtype dt, int head_dim);
+
+}  // namespace fav
