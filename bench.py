@@ -191,9 +191,20 @@ def oracle_sample(w, tensors, budget_s: float):
                 break
             qs, dys = q[cq[b]:cq[b + 1], n], dy[cq[b]:cq[b + 1], n]
             ks, vs = k[ck[b]:ck[b + 1], n // group], v[ck[b]:ck[b + 1], n // group]
+            keep_rows = None
+            if w.keep_prob < 1.0:
+                from varlen_flashattention_backward_gb300 import workloads as wl
+                off = int(oracle.mask_bit_offsets(w.lens, w.lens_kv, w.n_heads)[b])
+                base = off + n * w.lens[b] * w.lens_kv[b]
+                lk = w.lens_kv[b]
+                keep_rows = (lambda rows, base=base, lk=lk: wl.keep_bits(
+                    w.mask_seed, w.keep_prob,
+                    base + np.asarray(rows)[:, None] * lk + np.arange(lk)[None, :]).astype(float))
             t0 = time.perf_counter()
-            y, m, l = oracle.unit_forward(qs, ks, vs, w.scale, w.pre_tokens, w.next_tokens)
-            oracle.unit_backward(qs, ks, vs, dys, y, m, l, w.scale, w.pre_tokens, w.next_tokens)
+            y, m, l = oracle.unit_forward(qs, ks, vs, w.scale, w.pre_tokens, w.next_tokens,
+                                          keep_rows, w.keep_prob)
+            oracle.unit_backward(qs, ks, vs, dys, y, m, l, w.scale, w.pre_tokens, w.next_tokens,
+                                 keep_rows, w.keep_prob)
             secs += time.perf_counter() - t0
             flops += 10.0 * w.head_dim * allowed_pairs([w.lens[b]], [w.lens_kv[b]],
                                                        w.pre_tokens, w.next_tokens)
@@ -405,7 +416,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6])
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tcgen05"])
     ap.add_argument("--ref-budget", type=float, default=10.0,
                     help="seconds of oracle work per timed sample")

@@ -4,8 +4,8 @@ for fp32 and <= 2e-2 * max|ref| for 16-bit types.
 
 Small problems are compared element by element over the whole batch; the
 full-size workloads 3-5 are run in the launch configuration bench.py times
-(default kernel choice) and compared on sampled (sequence, head) units, with
-sum invariants checked over every unit."""
+(default kernel choice) and compared element by element on whole sampled
+(sequence, head) units, with sum invariants checked over every unit."""
 
 import math
 
@@ -19,7 +19,7 @@ from varlen_flashattention_backward_gb300 import build as fb
 from varlen_flashattention_backward_gb300 import workloads as wl
 
 from _helpers import (TOL, assert_close, device_mask, f64, gpu_forward_backward, oracle_full,
-                      rel_err, sampled_unit_check)
+                      rel_err, unit_check)
 
 pytestmark = pytest.mark.gpu
 BIG = wl.UNBOUNDED
@@ -199,17 +199,17 @@ def _invariants(w, out):
 
 @pytest.mark.parametrize("cid,units", [
     (3, "longest2+shortest1"),
-    (4, [(0, 0), (1, 7)]),
+    (4, [(1, 7)]),
     (5, [(1, 3)]),
 ])
-def test_full_size_sampled(cid, units):
+def test_full_size_sampled_units(cid, units):
     w, tensors, out = _full_size_run(cid)
     _invariants(w, out)
     if units == "longest2+shortest1":
         lo, hi = int(np.argmin(w.lens)), int(np.argmax(w.lens))
         units = [(hi, 0), (hi, w.n_heads - 1), (lo, 5)]
     for b, n in units:
-        errs = sampled_unit_check(w, tensors, out, b, n)
+        errs = unit_check(w, tensors, out, b, n)
         tol = TOL[w.dtype]
         assert errs["lse"] <= 1e-3, (b, n, errs)
         for k in ("y", "dq", "dk", "dv"):

@@ -14,6 +14,10 @@ The five workloads are the ones the library is measured and checked on:
 5. bf16, 4 x 16384 (T = 65536), N = 16, D = 128, sliding window
    preTokens = 4096 / nextTokens = 0, dropout keep_prob = 0.9.
 
+Workload 6 is the profiling case: bf16, 8 x 2048 (T = 16384), N = 16,
+D = 128, causal.  Its inputs (335 MB) exceed L2 while one backward launch
+stays well under a millisecond.
+
 Every workload uses scale = 1/sqrt(D).  Q, K, V and dY are drawn in fp32
 from one ``torch.Generator`` seeded with ``seed`` (order: lengths when they
 are random, then Q, K, V, dY) and rounded to the storage dtype.
@@ -123,6 +127,8 @@ def workload(cid: int, seed: int = 0) -> Workload:
         return Workload(4, "bf16", [32768, 32768], 8, 128, UNBOUNDED, 0, seed=seed)
     if cid == 5:
         return Workload(5, "bf16", [16384] * 4, 16, 128, 4096, 0, keep_prob=0.9, seed=seed)
+    if cid == 6:
+        return Workload(6, "bf16", [2048] * 8, 16, 128, UNBOUNDED, 0, seed=seed)
     raise ValueError(f"unknown workload {cid}")
 
 
