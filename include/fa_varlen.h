@@ -172,6 +172,39 @@ fa_status fa_varlen_bwd_ex(
     void *workspace, size_t workspace_bytes, fa_stream_t stream,
     const fa_bwd_options *options);
 
+/* fa_varlen_bwd for callers that cannot allocate device memory (no
+ * counterpart on the FAG-V2 page; an addition of this library).  Code that
+ * runs inside a custom allocator or a memory-pool callback, or a runtime
+ * that owns all device memory, may be unable to call cudaMalloc for a
+ * workspace.  This entry point takes none: its scratch is a 64 MiB array
+ * reserved by the library's CUDA module on every device that loads the
+ * library, held until the process exits.  It allocates nothing (no
+ * cudaMalloc, cudaFree or allocating library routine).
+ *   - Arguments, layout and results are those of fa_varlen_bwd.
+ *   - Problems whose workspace (fa_varlen_bwd_workspace_size) exceeds
+ *     64 MiB are rejected with FA_ERR_WORKSPACE before any launch.  Example:
+ *     the fp32 dQ accumulator alone takes total_q * head_num * head_dim * 4
+ *     bytes.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture on the device.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind; each call re-initialises what it needs.  Calls whose GPU work
+ *     overlaps (other streams, other host threads) race on the array and
+ *     give wrong results: serialise them.
+ *   - The error word it uses is internal; fa_varlen_read_error cannot read
+ *     it. */
+fa_status fa_varlen_bwd_static_scratch(
+    const void *q, const void *k, const void *v, const void *dy,
+    const uint8_t *drop_mask, int64_t drop_mask_bytes,
+    const float *softmax_max, const float *softmax_sum, const void *y,
+    const int64_t *seq_lens_q, const int64_t *seq_lens_kv, int64_t batch,
+    int64_t total_q, int64_t total_kv, int64_t head_num, int64_t head_num_kv,
+    int64_t head_dim, fa_dtype dtype, const char *layout, double scale,
+    double keep_prob, int64_t pre_tokens, int64_t next_tokens,
+    int64_t sparse_mode,
+    void *dq, void *dk, void *dv, fa_stream_t stream);
+
 /* Reads the error word that the last call on `workspace` left in it, after
  * synchronising `stream`: FA_OK, or FA_ERR_TIMEOUT when a bounded in-kernel
  * wait expired.  *code receives the raw word (0 = no error). */

@@ -59,6 +59,9 @@ _SIGS = {
                           ctypes.POINTER(BwdOptions)], _i32),
     "fa_varlen_read_error": ([_vp, _sz, _vp, ctypes.POINTER(ctypes.c_int32)], _i32),
     "fa_gen_keep_mask": ([_vp, _i64, ctypes.c_uint64, _f64, _vp], _i32),
+    "fa_varlen_bwd_static_scratch": ([_vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp] +
+                                     _SCALARS[:8] + [_i32, _cp, _f64, _f64, _i64, _i64, _i64,
+                                                     _vp, _vp, _vp, _vp], _i32),
     "fa_varlen_bwd_schedule": ([_pi64, _pi64, _i64, _i64, _i64, _i64, _i32,
                                 ctypes.POINTER(ctypes.c_int32), _i64, _pi64], _i32),
 }
@@ -205,6 +208,27 @@ def bwd(q, k, v, dy, y, softmax_max, softmax_sum, lens_q, lens_kv, scale, pre_to
                                   int(next_tokens), 0, _ptr(dq), _ptr(dk), _ptr(dv),
                                   _ptr(workspace), workspace.numel(), _stream(stream),
                                   ctypes.byref(opt)), "fa_varlen_bwd_ex")
+    return dq, dk, dv
+
+
+def bwd_static_scratch(q, k, v, dy, y, softmax_max, softmax_sum, lens_q, lens_kv, scale,
+                       pre_tokens, next_tokens, keep_prob=1.0, drop_mask=None, dq=None, dk=None,
+                       dv=None, stream=None):
+    """dQ, dK, dV through fa_varlen_bwd_static_scratch: no workspace is
+    allocated; the library's 64 MiB device array serves as scratch."""
+    tq, n, d = q.shape
+    n_kv = k.shape[1]
+    lq, b, _ = _lens(lens_q)
+    lk, _, _ = _lens(lens_kv)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    mask_bytes = 0 if drop_mask is None else drop_mask.numel()
+    _check(lib().fa_varlen_bwd_static_scratch(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(dy), _ptr(drop_mask), mask_bytes, _ptr(softmax_max),
+        _ptr(softmax_sum), _ptr(y), lq, lk, b, tq, k.shape[0], n, n_kv, d, _DTYPE[q.dtype],
+        b"TND", float(scale), float(keep_prob), int(pre_tokens), int(next_tokens), 0, _ptr(dq),
+        _ptr(dk), _ptr(dv), _stream(stream)), "fa_varlen_bwd_static_scratch")
     return dq, dk, dv
 
 
