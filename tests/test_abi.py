@@ -170,8 +170,18 @@ def test_schedule_covers_exactly_the_allowed_pairs(case, kv_tile):
     items = fa.bwd_schedule(lens, lens, nkv, pre, nxt, kv_tile)
     n_tiles = sum((L + kv_tile - 1) // kv_tile for L in lens) * nkv
     assert len(items) == n_tiles
-    counts = [c for *_, c in items]
-    assert counts == sorted(counts, reverse=True)          # longest first
+    # the items of one (sequence, head) unit are contiguous and longest first;
+    # units are ordered by their longest item, longest first
+    units = []
+    for b, h, t, lo, cnt in items:
+        if not units or units[-1][0] != (b, h):
+            units.append(((b, h), []))
+        units[-1][1].append(cnt)
+    assert len({u for u, _ in units}) == len(units)
+    for _, counts in units:
+        assert counts == sorted(counts, reverse=True)
+    heads = [counts[0] for _, counts in units]
+    assert heads == sorted(heads, reverse=True)
     seen = set()
     for b, h, t, lo, cnt in items:
         assert (b, h, t) not in seen

@@ -97,30 +97,53 @@ std::vector<SeqInfo> build_seqs(const Problem &pr) {
 // Backward work list: one item per (sequence, key/value head, key tile).  A
 // key tile [k0, k1) sees queries i with k0 - next <= i <= k1 - 1 + pre; only
 // the query tiles meeting that range are visited, so fully masked causal or
-// band tiles cost nothing.  Items are ordered longest first (LPT) so the
-// tail of the grid holds the short ones.
+// band tiles cost nothing.
+//
+// Order: the items of one (sequence, head) unit are contiguous, longest
+// first, and units are ordered by their longest item, longest first.  The
+// hardware dispatches CTAs in this order as SMs free up (greedy list
+// scheduling), so the tail of the grid holds short items, while the units
+// in flight at any moment stay few: their Q, dY and dQ accumulator rows
+// (about 1 MB each per 2048 tokens) stay resident in L2 across the key
+// tiles that re-read them.
 std::vector<WorkItem> build_bwd_items(const Problem &pr, int kv_tile) {
+  struct Unit {
+    size_t first, count;
+    int max_len;
+  };
   std::vector<WorkItem> items;
+  std::vector<Unit> units;
   for (int64_t b = 0; b < pr.batch; ++b) {
     const int64_t lq = pr.lens_q[b], lk = pr.lens_kv[b];
     const int64_t tiles = ceil_div(lk, kv_tile);
-    for (int64_t t = 0; t < tiles; ++t) {
-      const int64_t k0 = t * kv_tile, k1 = std::min(lk, k0 + kv_tile);
-      const int64_t lo = std::max<int64_t>(0, k0 - pr.next);
-      const int64_t hi = std::min<int64_t>(lq - 1, k1 - 1 + pr.pre);
-      int64_t qlo = 0, cnt = 0;
-      if (lq > 0 && lo <= hi) {
-        qlo = lo / kQTile;
-        cnt = hi / kQTile - qlo + 1;
-      }
-      for (int64_t h = 0; h < pr.n_kv; ++h)
+    for (int64_t h = 0; h < pr.n_kv; ++h) {
+      Unit u{items.size(), size_t(tiles), 0};
+      for (int64_t t = 0; t < tiles; ++t) {
+        const int64_t k0 = t * kv_tile, k1 = std::min(lk, k0 + kv_tile);
+        const int64_t lo = std::max<int64_t>(0, k0 - pr.next);
+        const int64_t hi = std::min<int64_t>(lq - 1, k1 - 1 + pr.pre);
+        int64_t qlo = 0, cnt = 0;
+        if (lq > 0 && lo <= hi) {
+          qlo = lo / kQTile;
+          cnt = hi / kQTile - qlo + 1;
+        }
         items.push_back({int32_t(b), int32_t(h), int32_t(t), int32_t(qlo | (cnt << 16))});
+        u.max_len = std::max(u.max_len, int(cnt));
+      }
+      std::stable_sort(items.begin() + u.first, items.end(),
+                       [](const WorkItem &a, const WorkItem &c) {
+                         return item_count(a) > item_count(c);
+                       });
+      if (tiles > 0) units.push_back(u);
     }
   }
-  std::stable_sort(items.begin(), items.end(), [](const WorkItem &a, const WorkItem &c) {
-    return item_count(a) > item_count(c);
-  });
-  return items;
+  std::stable_sort(units.begin(), units.end(),
+                   [](const Unit &a, const Unit &c) { return a.max_len > c.max_len; });
+  std::vector<WorkItem> out;
+  out.reserve(items.size());
+  for (const Unit &u : units)
+    out.insert(out.end(), items.begin() + u.first, items.begin() + u.first + u.count);
+  return out;
 }
 
 // Forward work list: one item per (sequence, query head, query tile) with the

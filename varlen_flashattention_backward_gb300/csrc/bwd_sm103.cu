@@ -23,7 +23,7 @@
 // in TMEM for the whole item and are written once at the end.
 //
 // Warp roles (16 warps):
-//   0      TMA producer: K, V once; Q, dY, lse, D per query tile (2 stages)
+//   0      TMA producer: K, V once; Q, dY, lse, D per query tile (3 stages)
 //   1      MMA issuer (one thread); the warp owns the TMEM allocation
 //   2-3    idle
 //   4-11   softmax: TMEM lane quarter = warp % 4 (one key per thread), column
@@ -54,7 +54,7 @@ using namespace sm103;
 constexpr int BN = kTcKvTile;   // 128 keys per item
 constexpr int BM = kQTile;      // 64 queries per iteration
 constexpr int HD = 128;         // head dim
-constexpr int STAGES = 2;
+constexpr int STAGES = 3;
 constexpr int NTHREADS = 512;
 
 // TMEM columns (512 allocated; 128 lanes x 32-bit cells).
@@ -223,17 +223,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_it > 0) {
-      tma_prefetch_map(&maps.q);
-      tma_prefetch_map(&maps.dy);
-      tma_prefetch_map(&maps.k);
-      tma_prefetch_map(&maps.v);
+    // The whole warp runs this loop; copies are issued by one elected lane.
+    if (n_it > 0) {
+      if (lane == 0) {
+        tma_prefetch_map(&maps.q);
+        tma_prefetch_map(&maps.dy);
+        tma_prefetch_map(&maps.k);
+        tma_prefetch_map(&maps.v);
+      }
+      __syncwarp();
       const int ky = sq.cu_k + k0, kx = kvh * HD;
-      mbar_arrive_expect_tx(bar(B_KV), 4 * 16384);
-      tma_load_2d(sb + SM_K, &maps.k, bar(B_KV), kx, ky);
-      tma_load_2d(sb + SM_K + 16384, &maps.k, bar(B_KV), kx + 64, ky);
-      tma_load_2d(sb + SM_V, &maps.v, bar(B_KV), kx, ky);
-      tma_load_2d(sb + SM_V + 16384, &maps.v, bar(B_KV), kx + 64, ky);
+      mbar_arrive_expect_tx_w(bar(B_KV), 4 * 16384);
+      tma_load_2d_w(sb + SM_K, &maps.k, bar(B_KV), kx, ky);
+      tma_load_2d_w(sb + SM_K + 16384, &maps.k, bar(B_KV), kx + 64, ky);
+      tma_load_2d_w(sb + SM_V, &maps.v, bar(B_KV), kx, ky);
+      tma_load_2d_w(sb + SM_V + 16384, &maps.v, bar(B_KV), kx + 64, ky);
       int issued = 0;
       for (int L = 0; L < n_it; ++L) {
         const int st = L % STAGES;
@@ -244,14 +248,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int q0 = (qlo + L % qcnt) * BM;
         const int qy = sq.cu_q + q0, qx = n * HD;
         const uint32_t full = bar(B_FULL + st);
-        mbar_arrive_expect_tx(full, 4 * 8192 + 2 * 256);
-        tma_load_2d(sb + SM_Q + st * 16384, &maps.q, full, qx, qy);
-        tma_load_2d(sb + SM_Q + st * 16384 + 8192, &maps.q, full, qx + 64, qy);
-        tma_load_2d(sb + SM_DY + st * 16384, &maps.dy, full, qx, qy);
-        tma_load_2d(sb + SM_DY + st * 16384 + 8192, &maps.dy, full, qx + 64, qy);
         const int64_t srow = int64_t(n) * p.tp + sq.qpad + q0;
-        bulk_load(sb + SM_LSE + st * 256, p.lse2 + srow, 256, full);
-        bulk_load(sb + SM_DSUM + st * 256, p.dsum + srow, 256, full);
+        mbar_arrive_expect_tx_w(full, 4 * 8192 + 2 * 256);
+        tma_load_2d_w(sb + SM_Q + st * 16384, &maps.q, full, qx, qy);
+        tma_load_2d_w(sb + SM_Q + st * 16384 + 8192, &maps.q, full, qx + 64, qy);
+        tma_load_2d_w(sb + SM_DY + st * 16384, &maps.dy, full, qx, qy);
+        tma_load_2d_w(sb + SM_DY + st * 16384 + 8192, &maps.dy, full, qx + 64, qy);
+        bulk_load_w(sb + SM_LSE + st * 256, p.lse2 + srow, 256, full);
+        bulk_load_w(sb + SM_DSUM + st * 256, p.dsum + srow, 256, full);
         ++issued;
       }
       // No copy may still be writing shared memory when the CTA exits.
@@ -262,45 +266,52 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_it > 0) {
+    // The whole warp runs this loop; each MMA and commit is issued by one
+    // elected lane from straight-line code (see mma_ss_w).
+    if (n_it > 0) {
       const uint32_t id_s = idesc_f16(128, BM, false, false, kBF16);   // S^T, dP^T
       const uint32_t id_g = idesc_f16(128, HD, false, true, kBF16);    // dV, dK
       const uint32_t id_q = idesc_f16(128, BM, true, true, kBF16);     // dQ^T
-      auto mma_kt = [&](uint32_t a_base, uint32_t b_base, uint32_t dcol) {
+      // Descriptors are built once per operand; a k-step adds its byte offset
+      // >> 4 to the 14-bit start-address field (shared addresses stay below
+      // 256 KB, so the field never carries).
+      const uint64_t dk_ = sdesc_sw128(sb + SM_K, 16, 1024);     // K, K-major
+      const uint64_t dv_ = sdesc_sw128(sb + SM_V, 16, 1024);     // V, K-major
+      const uint64_t dkt = sdesc_sw128(sb + SM_K, 16384, 1024);  // K, MN-major (K^T)
+      const uint64_t dds = sdesc_sw128(sb + SM_DS, 16384, 1024); // dS^T, MN-major
+      auto mma_kt = [&](uint64_t a0, uint32_t b_base, uint32_t dcol) {
         // D[128 x 64] = A[128 x 128] B[64 x 128]^T, both K-major (2 boxes along K)
+        const uint64_t b0 = sdesc_sw128(b_base, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk & 3) * 32;
-          const uint64_t a = sdesc_sw128(a_base + (kk >> 2) * 16384 + off, 16, 1024);
-          const uint64_t b = sdesc_sw128(b_base + (kk >> 2) * 8192 + off, 16, 1024);
-          mma_ss(tmem + dcol, a, b, id_s, kk > 0 ? 1u : 0u);
+          mma_ss_w(tmem + dcol, a0 + (((kk >> 2) * 16384 + off) >> 4),
+                   b0 + (((kk >> 2) * 8192 + off) >> 4), id_s, kk > 0 ? 1u : 0u);
         }
       };
-      auto mma_grad = [&](uint32_t a_col, uint32_t b_base, uint32_t dcol, bool acc) {
+      auto mma_grad = [&](uint32_t a_col, uint32_t b_base, uint32_t dcol, uint32_t acc) {
         // D[128 x 128] += A[128 x 64] (TMEM) B[64 x 128] (MN-major)
+        const uint64_t b0 = sdesc_sw128(b_base, 8192, 1024);
+        mma_ts_w(tmem + dcol, tmem + a_col, b0, id_g, acc);
 #pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk) {
-          const uint64_t b = sdesc_sw128(b_base + kk * 2048, 8192, 1024);
-          mma_ts(tmem + dcol, tmem + a_col + kk * 8, b, id_g, (acc || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 1; kk < BM / 16; ++kk)
+          mma_ts_w(tmem + dcol, tmem + a_col + kk * 8, b0 + ((kk * 2048) >> 4), id_g, 1u);
       };
       auto mma_dq = [&]() {
         // dQ^T[128 d x 64 q] = K^T[128 d x 128 keys] dS^T[128 keys x 64 q]
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t a = sdesc_sw128(sb + SM_K + kk * 2048, 16384, 1024);
-          const uint64_t b = sdesc_sw128(sb + SM_DS + kk * 2048, 16384, 1024);
-          mma_ss(tmem + COL_DQ, a, b, id_q, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ss_w(tmem + COL_DQ, dkt + ((kk * 2048) >> 4), dds + ((kk * 2048) >> 4), id_q,
+                   kk > 0 ? 1u : 0u);
       };
       bool ok = wait_or_abort(ctl, bar(B_KV), 0, ROLE_MMA) &&
                 wait_or_abort(ctl, bar(B_FULL), 0, ROLE_MMA);
       tc_fence_after();
       if (ok) {
-        mma_kt(sb + SM_K, sb + SM_Q, COL_S);
-        mma_commit(bar(B_SFULL));
-        mma_kt(sb + SM_V, sb + SM_DY, COL_DP);
-        mma_commit(bar(B_DPFULL));
+        mma_kt(dk_, sb + SM_Q, COL_S);
+        mma_commit_w(bar(B_SFULL));
+        mma_kt(dv_, sb + SM_DY, COL_DP);
+        mma_commit_w(bar(B_DPFULL));
       }
       for (int L = 0; ok && L < n_it; ++L) {
         const int st = L % STAGES;
@@ -310,32 +321,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                wait_or_abort(ctl, bar(B_SFREE), L & 1, ROLE_MMA);
           if (!ok) break;
           tc_fence_after();
-          mma_kt(sb + SM_K, sb + SM_Q + s1 * 16384, COL_S);
-          mma_commit(bar(B_SFULL));
+          mma_kt(dk_, sb + SM_Q + s1 * 16384, COL_S);
+          mma_commit_w(bar(B_SFULL));
         }
         if (!(ok = wait_or_abort(ctl, bar(B_PFULL), L & 1, ROLE_MMA))) break;
         tc_fence_after();
-        mma_grad(COL_P, sb + SM_DY + st * 16384, COL_DV, L > 0);
-        mma_commit(bar(B_PFREE));
+        mma_grad(COL_P, sb + SM_DY + st * 16384, COL_DV, L > 0 ? 1u : 0u);
+        mma_commit_w(bar(B_PFREE));
         if (!(ok = wait_or_abort(ctl, bar(B_DSFULL), L & 1, ROLE_MMA))) break;
         tc_fence_after();
-        mma_grad(COL_DS, sb + SM_Q + st * 16384, COL_DK, L > 0);
+        mma_grad(COL_DS, sb + SM_Q + st * 16384, COL_DK, L > 0 ? 1u : 0u);
         if (L > 0 && !(ok = wait_or_abort(ctl, bar(B_DQFREE), (L - 1) & 1, ROLE_MMA))) break;
         tc_fence_after();
         mma_dq();
-        mma_commit(bar(B_DQFULL));
-        mma_commit(bar(B_DSFREE));
-        mma_commit(bar(B_EMPTY + st));
+        mma_commit_w(bar(B_DQFULL));
+        mma_commit_w(bar(B_DSFREE));
+        mma_commit_w(bar(B_EMPTY + st));
         if (L + 1 < n_it) {
           if (!(ok = wait_or_abort(ctl, bar(B_DPFREE), L & 1, ROLE_MMA))) break;
           tc_fence_after();
-          mma_kt(sb + SM_V, sb + SM_DY + ((L + 1) % STAGES) * 16384, COL_DP);
-          mma_commit(bar(B_DPFULL));
+          mma_kt(dv_, sb + SM_DY + ((L + 1) % STAGES) * 16384, COL_DP);
+          mma_commit_w(bar(B_DPFULL));
         }
       }
-      if (ok) mma_commit(bar(B_ACC));
+      if (ok) mma_commit_w(bar(B_ACC));
       // Every MMA of this CTA has finished before TMEM is freed.
-      mma_commit(bar(B_FINAL));
+      mma_commit_w(bar(B_FINAL));
       const int never = 0;
       mbar_wait(bar(B_FINAL), 0, p.timeout_ns, &never);
     }
@@ -359,9 +370,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tmem_ld32(tmem + lane_off + COL_S + 32 * half, r);
       tc_fence_before();
       if (lane == 0) mbar_arrive(bar(B_SFREE));
-      const float *lse = reinterpret_cast<const float *>(sm + SM_LSE + st * 256) + 32 * half;
+      {
+        const uint32_t lse_addr = sb + SM_LSE + st * 256 + 128 * half;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) pr[c] = ex2(fmaf(__uint_as_float(r[c]), sl2, -lse[c]));
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 l4 = ld_shared_f4(lse_addr + 16 * c4);
+          pr[4 * c4 + 0] = ex2(fmaf(__uint_as_float(r[4 * c4 + 0]), sl2, -l4.x));
+          pr[4 * c4 + 1] = ex2(fmaf(__uint_as_float(r[4 * c4 + 1]), sl2, -l4.y));
+          pr[4 * c4 + 2] = ex2(fmaf(__uint_as_float(r[4 * c4 + 2]), sl2, -l4.z));
+          pr[4 * c4 + 3] = ex2(fmaf(__uint_as_float(r[4 * c4 + 3]), sl2, -l4.w));
+        }
+      }
       const bool full_tile = (k0 + BN - 1 <= q0 + p.next) && (k0 >= q0 + BM - 1 - p.pre) &&
                              (k0 + BN <= sq.len_k);
       if (!full_tile) {
@@ -404,14 +423,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tmem_ld32(tmem + lane_off + COL_DP + 32 * half, r);
       tc_fence_before();
       if (lane == 0) mbar_arrive(bar(B_DPFREE));
-      const float *dsum = reinterpret_cast<const float *>(sm + SM_DSUM + st * 256) + 32 * half;
+      {
+        const uint32_t dsum_addr = sb + SM_DSUM + st * 256 + 128 * half;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float z0 = ((keep >> (2 * c)) & 1u) ? zs : 0.f;
-        const float z1 = ((keep >> (2 * c + 1)) & 1u) ? zs : 0.f;
-        const float d0 = pr[2 * c] * (__uint_as_float(r[2 * c]) * z0 - dsum[2 * c]);
-        const float d1 = pr[2 * c + 1] * (__uint_as_float(r[2 * c + 1]) * z1 - dsum[2 * c + 1]);
-        pk[c] = pack2<kBF16>(d0, d1);
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 d4 = ld_shared_f4(dsum_addr + 16 * c4);
+          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+          float ds[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = 4 * c4 + e;
+            const float z = ((keep >> c) & 1u) ? zs : 0.f;
+            ds[e] = pr[c] * (__uint_as_float(r[c]) * z - dv[e]);
+          }
+          pk[2 * c4] = pack2<kBF16>(ds[0], ds[1]);
+          pk[2 * c4 + 1] = pack2<kBF16>(ds[2], ds[3]);
+        }
       }
       if (L > 0 && !wait_or_abort(ctl, bar(B_DSFREE), (L - 1) & 1, ROLE_SOFTMAX)) break;
       tc_fence_after();
@@ -478,13 +505,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_before();
       if (lane == 0) mbar_arrive(bar(B_DQFREE));
       const int rows = min(BM, sq.len_q - q0);
-      float *base = p.dq_acc + (int64_t(sq.cu_q) + q0) * row_stride + int64_t(n) * HD + d;
+      float *ptr = p.dq_acc + (int64_t(sq.cu_q) + q0) * row_stride + int64_t(n) * HD + d;
 #pragma unroll
-      for (int c = 0; c < 32; ++c)
-        if (c < rows) red_add_f32(base + c * row_stride, __uint_as_float(a[c]));
+      for (int c = 0; c < 32; ++c, ptr += row_stride)
+        if (c < rows) red_add_f32(ptr, __uint_as_float(a[c]));
 #pragma unroll
-      for (int c = 0; c < 32; ++c)
-        if (32 + c < rows) red_add_f32(base + (32 + c) * row_stride, __uint_as_float(b[c]));
+      for (int c = 0; c < 32; ++c, ptr += row_stride)
+        if (32 + c < rows) red_add_f32(ptr, __uint_as_float(b[c]));
     }
   }
 
