@@ -136,8 +136,10 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return kBF16 ? pack_bf16(lo, hi) : pack_f16(lo, hi);
 }
 
-__device__ __forceinline__ void red_add_f32(float *addr, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+__device__ __forceinline__ void red_add_v4_f32(float *addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -491,7 +493,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else if (warp >= 12) {
     // ------------------------------------------------------------ dQ drain
     const int quarter = warp & 3;
-    const int d = quarter * 32 + lane;
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
     const int64_t row_stride = int64_t(p.n) * HD;
     for (int L = 0; L < n_it; ++L) {
@@ -504,14 +505,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tmem_ld32(tmem + lane_off + COL_DQ + 32, b);
       tc_fence_before();
       if (lane == 0) mbar_arrive(bar(B_DQFREE));
+      // Thread (quad m, c) holds column d = quarter*32 + 4m + c for 64 queries.
+      // A 4 x 4 transpose inside each quad (two xor-shuffle rounds) gives it
+      // d = quarter*32 + 4m + 0..3 at query 4j + c, so that each reduction
+      // adds 16 contiguous bytes (4x fewer reduction instructions).
       const int rows = min(BM, sq.len_q - q0);
-      float *ptr = p.dq_acc + (int64_t(sq.cu_q) + q0) * row_stride + int64_t(n) * HD + d;
+      const int c = lane & 3;
+      float *ptr = p.dq_acc + (int64_t(sq.cu_q) + q0 + c) * row_stride + int64_t(n) * HD +
+                   quarter * 32 + (lane & ~3);
 #pragma unroll
-      for (int c = 0; c < 32; ++c, ptr += row_stride)
-        if (c < rows) red_add_f32(ptr, __uint_as_float(a[c]));
-#pragma unroll
-      for (int c = 0; c < 32; ++c, ptr += row_stride)
-        if (32 + c < rows) red_add_f32(ptr, __uint_as_float(b[c]));
+      for (int j = 0; j < BM / 4; ++j, ptr += 4 * row_stride) {
+        const uint32_t *src = j < 8 ? a : b;
+        const int o = 4 * (j & 7);
+        const float x0 = __uint_as_float(src[o]), x1 = __uint_as_float(src[o + 1]);
+        const float x2 = __uint_as_float(src[o + 2]), x3 = __uint_as_float(src[o + 3]);
+        const bool hi2 = c & 2, hi1 = c & 1;
+        const float t0 = __shfl_xor_sync(0xffffffffu, hi2 ? x0 : x2, 2);
+        const float t1 = __shfl_xor_sync(0xffffffffu, hi2 ? x1 : x3, 2);
+        const float r0 = hi2 ? t0 : x0, r1 = hi2 ? t1 : x1;
+        const float r2 = hi2 ? x2 : t0, r3 = hi2 ? x3 : t1;
+        const float u0 = __shfl_xor_sync(0xffffffffu, hi1 ? r0 : r1, 1);
+        const float u1 = __shfl_xor_sync(0xffffffffu, hi1 ? r2 : r3, 1);
+        if (4 * j + c < rows)
+          red_add_v4_f32(ptr, hi1 ? u0 : r0, hi1 ? r1 : u0, hi1 ? u1 : r2, hi1 ? r3 : u1);
+      }
     }
   }
 
