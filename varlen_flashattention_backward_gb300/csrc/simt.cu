@@ -20,6 +20,86 @@ constexpr float kLog2e = 1.4426950408889634f;
 // preprocess: D_i = sum_d dY * Y, lse2_i = (max_i + ln sum_i) * log2(e),
 // dq_acc row := 0.  One block per (64-row padded query tile, head).
 // ---------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ float dot16(uint4 a, uint4 b) {
+  const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+  float acc = 0.f;
+  if constexpr (sizeof(T) == 4) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc = fmaf(__uint_as_float(av[k]), __uint_as_float(bv[k]), acc);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const T *ah = reinterpret_cast<const T *>(&av[k]);
+      const T *bh = reinterpret_cast<const T *>(&bv[k]);
+      acc = fmaf(to_f(ah[0]), to_f(bh[0]), acc);
+      acc = fmaf(to_f(ah[1]), to_f(bh[1]), acc);
+    }
+  }
+  return acc;
+}
+
+// Rows are read with 16-byte loads, D / (16 / sizeof(T)) lanes per row and
+// several rows per warp instruction; every load of a warp's rows is issued
+// before the reductions.  Needs 16-byte aligned dY and Y (the launcher
+// checks; otherwise preprocess_kernel below runs).
+template <typename T, int D>
+__global__ void __launch_bounds__(256) preprocess_vec_kernel(BwdParams p) {
+  constexpr int kVec = 16 / int(sizeof(T));
+  constexpr int kLanes = D / kVec;
+  constexpr int kRowsPass = 32 / kLanes;
+  constexpr int kRowsWarp = kQTile / 8;
+  constexpr int kPasses = kRowsWarp / kRowsPass;
+  const int tile = blockIdx.x, n = blockIdx.y;
+  const int row0 = tile * kQTile;
+  const int b = seq_of_padded_row(p.seqs, p.batch, row0);
+  const SeqInfo s = p.seqs[b];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane / kLanes, part = lane % kLanes;
+  const uint4 *dy = static_cast<const uint4 *>(p.dy);
+  const uint4 *y = static_cast<const uint4 *>(p.y);
+  uint4 a[kPasses], c[kPasses];
+#pragma unroll
+  for (int k = 0; k < kPasses; ++k) {
+    const int i = row0 + warp * kRowsWarp + k * kRowsPass + sub - s.qpad;
+    a[k] = c[k] = make_uint4(0u, 0u, 0u, 0u);
+    if (i < s.len_q) {
+      const int64_t e = ((int64_t(s.cu_q) + i) * p.n + n) * (D / kVec) + part;
+      a[k] = __ldg(dy + e);
+      c[k] = __ldg(y + e);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kPasses; ++k) {
+    const int prow = row0 + warp * kRowsWarp + k * kRowsPass + sub;
+    const int i = prow - s.qpad;
+    float acc = dot16<T>(a[k], c[k]);
+#pragma unroll
+    for (int o = kLanes / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (part == 0) {
+      float lse2 = CUDART_INF_F;
+      if (i < s.len_q) {
+        const int64_t t = int64_t(s.cu_q) + i;
+        const float m = p.smax[(t * p.n + n) * 8];
+        const float l = p.ssum[(t * p.n + n) * 8];
+        if (l > 0.f && m > -CUDART_INF_F) lse2 = (m + logf(l)) * kLog2e;
+      } else {
+        acc = 0.f;
+      }
+      p.lse2[int64_t(n) * p.tp + prow] = lse2;
+      p.dsum[int64_t(n) * p.tp + prow] = acc;
+    }
+  }
+  for (int e = threadIdx.x; e < kQTile * (D / 4); e += 256) {
+    const int r = e / (D / 4), c4 = e % (D / 4);
+    const int i = row0 + r - s.qpad;
+    if (i < s.len_q)
+      reinterpret_cast<float4 *>(p.dq_acc + ((int64_t(s.cu_q) + i) * p.n + n) * D)[c4] =
+          make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// Same results for any alignment: one warp per row.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) preprocess_kernel(BwdParams p) {
   const int tile = blockIdx.x, n = blockIdx.y;
@@ -452,7 +532,10 @@ cudaError_t launch_fwd_simt_t(const FwdParams &p, cudaStream_t st) {
 template <typename T, int D>
 cudaError_t launch_pre_t(const BwdParams &p, cudaStream_t st) {
   dim3 grid(p.tp / kQTile, p.n);
-  preprocess_kernel<T, D><<<grid, 256, 0, st>>>(p);
+  if (((reinterpret_cast<uintptr_t>(p.dy) | reinterpret_cast<uintptr_t>(p.y)) & 15u) == 0)
+    preprocess_vec_kernel<T, D><<<grid, 256, 0, st>>>(p);
+  else
+    preprocess_kernel<T, D><<<grid, 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -317,6 +317,18 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   return r;
 }
 
+// Paired fp32 arithmetic: one instruction does the work of two lanes.
+// (dx, dy) = (ax, ay) * (bx, by) + (cx, cy);  = (ax, ay) - (bx, by);  = (ax, ay) * (bx, by).
+__device__ __forceinline__ void fma2(float &dx, float &dy, float ax, float ay, float bx, float by, float cx, float cy) {
+  asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\tfma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}" : "=f"(dx), "=f"(dy) : "f"(ax), "f"(ay), "f"(bx), "f"(by), "f"(cx), "f"(cy));
+}
+__device__ __forceinline__ void sub2(float &dx, float &dy, float ax, float ay, float bx, float by) {
+  asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tsub.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}" : "=f"(dx), "=f"(dy) : "f"(ax), "f"(ay), "f"(bx), "f"(by));
+}
+__device__ __forceinline__ void mul2(float &dx, float &dy, float ax, float ay, float bx, float by) {
+  asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}" : "=f"(dx), "=f"(dy) : "f"(ax), "f"(ay), "f"(bx), "f"(by));
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
