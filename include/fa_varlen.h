@@ -211,6 +211,19 @@ fa_status fa_varlen_bwd_static_scratch(
 fa_status fa_varlen_read_error(const void *workspace, size_t workspace_bytes,
                                fa_stream_t stream, int32_t *code);
 
+/* Self-test of the in-kernel failure detection, with no GPU fault involved.
+ * Launches one small kernel whose threads wait, through the same bounded
+ * wait the backward kernel uses, on an mbarrier phase that nothing ever
+ * completes.  The wait gives up after wait_timeout_ns, records its timeout
+ * code in the error word at the start of `workspace` (device memory, at
+ * least 256 bytes; the word is cleared first) as a stalled backward would,
+ * and the kernel returns normally, so the context stays usable.  Read the
+ * outcome with fa_varlen_read_error, which then returns FA_ERR_TIMEOUT.
+ * Errors: FA_ERR_NULLPTR (workspace), FA_ERR_WORKSPACE (< 256 bytes),
+ * FA_ERR_INVALID (wait_timeout_ns outside [1000, 10^10]), FA_ERR_CUDA. */
+fa_status fa_varlen_selftest_wait_timeout(void *workspace, size_t workspace_bytes,
+                                          int64_t wait_timeout_ns, fa_stream_t stream);
+
 /* Human-readable name of a status. */
 const char *fa_status_string(fa_status status);
 

@@ -198,3 +198,12 @@ def test_schedule_covers_exactly_the_allowed_pairs(case, kv_tile):
         # ... and no visited query tile is entirely masked for this key tile
         for qt in range(lo, lo + cnt):
             assert cols[qt * 64:(qt + 1) * 64].any(), (b, t, qt)
+
+
+def test_selftest_argument_checks():
+    L = fa.lib()
+    fake = ctypes.c_void_p(0x1000)
+    assert L.fa_varlen_selftest_wait_timeout(None, 256, 10**6, None) == fa.FA_ERR_NULLPTR
+    assert L.fa_varlen_selftest_wait_timeout(fake, 64, 10**6, None) == fa.FA_ERR_WORKSPACE
+    assert L.fa_varlen_selftest_wait_timeout(fake, 256, 10, None) == fa.FA_ERR_INVALID
+    assert L.fa_varlen_selftest_wait_timeout(fake, 256, 10**11, None) == fa.FA_ERR_INVALID

@@ -62,6 +62,7 @@ _SIGS = {
     "fa_varlen_bwd_static_scratch": ([_vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp] +
                                      _SCALARS[:8] + [_i32, _cp, _f64, _f64, _i64, _i64, _i64,
                                                      _vp, _vp, _vp, _vp], _i32),
+    "fa_varlen_selftest_wait_timeout": ([_vp, _sz, _i64, _vp], _i32),
     "fa_varlen_bwd_schedule": ([_pi64, _pi64, _i64, _i64, _i64, _i64, _i32,
                                 ctypes.POINTER(ctypes.c_int32), _i64, _pi64], _i32),
 }
@@ -230,6 +231,14 @@ def bwd_static_scratch(q, k, v, dy, y, softmax_max, softmax_sum, lens_q, lens_kv
         b"TND", float(scale), float(keep_prob), int(pre_tokens), int(next_tokens), 0, _ptr(dq),
         _ptr(dk), _ptr(dv), _stream(stream)), "fa_varlen_bwd_static_scratch")
     return dq, dk, dv
+
+
+def selftest_wait_timeout(workspace, wait_timeout_ns, stream=None):
+    """fa_varlen_selftest_wait_timeout: a kernel whose bounded wait on a
+    barrier nothing completes must expire and record a timeout code."""
+    _check(lib().fa_varlen_selftest_wait_timeout(_ptr(workspace), workspace.numel(),
+                                                 int(wait_timeout_ns), _stream(stream)),
+           "fa_varlen_selftest_wait_timeout")
 
 
 def read_error(workspace, stream=None) -> int:

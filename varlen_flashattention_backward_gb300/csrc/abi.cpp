@@ -508,6 +508,17 @@ fa_status fa_varlen_bwd_schedule(const int64_t *seq_lens_q, const int64_t *seq_l
   return FA_OK;
 }
 
+fa_status fa_varlen_selftest_wait_timeout(void *workspace, size_t workspace_bytes,
+                                          int64_t wait_timeout_ns, fa_stream_t stream) {
+  if (workspace == nullptr) return FA_ERR_NULLPTR;
+  if (workspace_bytes < kHeaderBytes) return FA_ERR_WORKSPACE;
+  if (wait_timeout_ns < 1000 || wait_timeout_ns > 10000000000LL) return FA_ERR_INVALID;
+  if (launch_wait_timeout_selftest(static_cast<int32_t *>(workspace), wait_timeout_ns,
+                                   reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
+}
+
 fa_status fa_gen_keep_mask(uint8_t *mask, int64_t nbits, uint64_t seed, double keep_prob,
                            fa_stream_t stream) {
   if (mask == nullptr) return FA_ERR_NULLPTR;

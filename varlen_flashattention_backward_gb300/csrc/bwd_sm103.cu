@@ -87,7 +87,10 @@ enum : int {
 };
 static_assert(B_COUNT * 8 <= 256, "barrier area");
 
-enum : int { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_SOFTMAX = 3, ROLE_DQ = 4, ROLE_EPILOGUE = 5 };
+enum : int {
+  ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_SOFTMAX = 3, ROLE_DQ = 4, ROLE_EPILOGUE = 5,
+  ROLE_SELFTEST = 7
+};
 
 struct TcMaps {
   CUtensorMap q, dy, k, v;
@@ -192,6 +195,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int qlo = item_lo(item), qcnt = item_count(item);
   const int n_it = qcnt * group;
   Ctl ctl{&s_abort, p.err, p.timeout_ns};
+  // Waits for this CTA's own copies and MMAs in flight (which finish without
+  // help from any other role) are bounded by at least a second, whatever
+  // the caller's timeout, so that no CTA exits while they still write.
+  const long long drain_ns = p.timeout_ns > 1000000000LL ? p.timeout_ns : 1000000000LL;
 
   if (threadIdx.x == 0) {
     s_abort = 0;
@@ -262,9 +269,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       // No copy may still be writing shared memory when the CTA exits.
       const int never = 0;
-      mbar_wait(bar(B_KV), 0, p.timeout_ns, &never);
+      mbar_wait(bar(B_KV), 0, drain_ns, &never);
       for (int L = issued > STAGES ? issued - STAGES : 0; L < issued; ++L)
-        mbar_wait(bar(B_FULL + L % STAGES), (L / STAGES) & 1, p.timeout_ns, &never);
+        mbar_wait(bar(B_FULL + L % STAGES), (L / STAGES) & 1, drain_ns, &never);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -350,7 +357,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // Every MMA of this CTA has finished before TMEM is freed.
       mma_commit_w(bar(B_FINAL));
       const int never = 0;
-      mbar_wait(bar(B_FINAL), 0, p.timeout_ns, &never);
+      mbar_wait(bar(B_FINAL), 0, drain_ns, &never);
     }
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ softmax / dS
@@ -377,10 +384,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 l4 = ld_shared_f4(lse_addr + 16 * c4);
-          pr[4 * c4 + 0] = ex2(fmaf(__uint_as_float(r[4 * c4 + 0]), sl2, -l4.x));
-          pr[4 * c4 + 1] = ex2(fmaf(__uint_as_float(r[4 * c4 + 1]), sl2, -l4.y));
-          pr[4 * c4 + 2] = ex2(fmaf(__uint_as_float(r[4 * c4 + 2]), sl2, -l4.z));
-          pr[4 * c4 + 3] = ex2(fmaf(__uint_as_float(r[4 * c4 + 3]), sl2, -l4.w));
+          fma2(pr[4 * c4], pr[4 * c4 + 1], __uint_as_float(r[4 * c4]), __uint_as_float(r[4 * c4 + 1]), sl2, sl2, -l4.x, -l4.y);
+          fma2(pr[4 * c4 + 2], pr[4 * c4 + 3], __uint_as_float(r[4 * c4 + 2]), __uint_as_float(r[4 * c4 + 3]), sl2, sl2, -l4.z, -l4.w);
+          pr[4 * c4 + 0] = ex2(pr[4 * c4 + 0]);
+          pr[4 * c4 + 1] = ex2(pr[4 * c4 + 1]);
+          pr[4 * c4 + 2] = ex2(pr[4 * c4 + 2]);
+          pr[4 * c4 + 3] = ex2(pr[4 * c4 + 3]);
         }
       }
       const bool full_tile = (k0 + BN - 1 <= q0 + p.next) && (k0 >= q0 + BM - 1 - p.pre) &&
@@ -406,11 +415,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         zs = p.inv_keep;
       }
       uint32_t pk[16];
+      if (p.use_dropout) {
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float a = ((keep >> (2 * c)) & 1u) ? pr[2 * c] * zs : 0.f;
-        const float b = ((keep >> (2 * c + 1)) & 1u) ? pr[2 * c + 1] * zs : 0.f;
-        pk[c] = pack2<kBF16>(a, b);
+        for (int c = 0; c < 16; ++c) {
+          const float a = ((keep >> (2 * c)) & 1u) ? pr[2 * c] * zs : 0.f;
+          const float b = ((keep >> (2 * c + 1)) & 1u) ? pr[2 * c + 1] * zs : 0.f;
+          pk[c] = pack2<kBF16>(a, b);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) pk[c] = pack2<kBF16>(pr[2 * c], pr[2 * c + 1]);
       }
       if (L > 0 && !wait_or_abort(ctl, bar(B_PFREE), (L - 1) & 1, ROLE_SOFTMAX)) break;
       tc_fence_after();
@@ -432,11 +446,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const float4 d4 = ld_shared_f4(dsum_addr + 16 * c4);
           const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
           float ds[4];
+          if (p.use_dropout) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = 4 * c4 + e;
-            const float z = ((keep >> c) & 1u) ? zs : 0.f;
-            ds[e] = pr[c] * (__uint_as_float(r[c]) * z - dv[e]);
+            for (int e = 0; e < 4; ++e) {
+              const int c = 4 * c4 + e;
+              const float z = ((keep >> c) & 1u) ? zs : 0.f;
+              ds[e] = pr[c] * (__uint_as_float(r[c]) * z - dv[e]);
+            }
+          } else {
+            sub2(ds[0], ds[1], __uint_as_float(r[4 * c4]), __uint_as_float(r[4 * c4 + 1]), dv[0], dv[1]);
+            sub2(ds[2], ds[3], __uint_as_float(r[4 * c4 + 2]), __uint_as_float(r[4 * c4 + 3]), dv[2], dv[3]);
+            mul2(ds[0], ds[1], ds[0], ds[1], pr[4 * c4], pr[4 * c4 + 1]);
+            mul2(ds[2], ds[3], ds[2], ds[3], pr[4 * c4 + 2], pr[4 * c4 + 3]);
           }
           pk[2 * c4] = pack2<kBF16>(ds[0], ds[1]);
           pk[2 * c4 + 1] = pack2<kBF16>(ds[2], ds[3]);
@@ -540,6 +561,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
 }
 
+// Failure-detection self-test: every thread waits, with the backward's
+// bounded wait, for a phase of an mbarrier that nothing arrives on.  The
+// wait expires, records kErrTimeoutBase + ROLE_SELFTEST in *err, and the
+// kernel ends normally.
+__global__ void wait_timeout_selftest_kernel(int32_t *err, long long timeout_ns) {
+  __shared__ uint64_t bar_word;
+  __shared__ int abort_flag;
+  const uint32_t b = smem_u32(&bar_word);
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(b, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  Ctl ctl{&abort_flag, err, timeout_ns};
+  wait_or_abort(ctl, b, 0, ROLE_SELFTEST);
+  __syncthreads();
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -592,6 +632,13 @@ cudaError_t launch_t(const BwdParams &p, cudaStream_t st) {
 }
 
 }  // namespace
+
+cudaError_t launch_wait_timeout_selftest(int32_t *err, long long timeout_ns, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int32_t), s);
+  if (e != cudaSuccess) return e;
+  wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(err, timeout_ns);
+  return cudaGetLastError();
+}
 
 bool tcgen05_supported(fa_dtype dt, int head_dim) {
   return head_dim == HD && (dt == FA_DTYPE_BF16 || dt == FA_DTYPE_FP16);

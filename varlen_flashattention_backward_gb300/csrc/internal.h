@@ -86,5 +86,6 @@ cudaError_t launch_fwd_simt(const FwdParams &p, fa_dtype dt, cudaStream_t s);
 cudaError_t launch_gen_keep_mask(uint8_t *mask, int64_t nbits, uint64_t seed,
                                  uint64_t threshold, int keep_all, cudaStream_t s);
 bool tcgen05_supported(fa_dtype dt, int head_dim);
+cudaError_t launch_wait_timeout_selftest(int32_t *err, long long timeout_ns, cudaStream_t s);
 
 }  // namespace fav
