@@ -97,7 +97,16 @@ typedef enum { FA_BWD_AUTO = 0, FA_BWD_SIMT = 1, FA_BWD_TCGEN05 = 2 } fa_bwd_imp
 
 typedef struct {
   int32_t impl;            /* fa_bwd_impl */
-  int32_t deterministic;   /* reserved, must be 0 */
+  /* Nonzero: bitwise-reproducible dq.  Each CTA takes its work item from a
+   * ticket counter in the workspace header, the items of one (sequence,
+   * head) unit run in ascending key-tile order, and the dq partial of every
+   * (query head, 64-row query tile) is added in ascending key-tile order,
+   * each adder waiting (bounded by wait_timeout_ns) on a per-tile counter
+   * for the one before it.  A CTA waits only on items taken before its own,
+   * so the waits always end.  dk and dv are deterministic in either mode.
+   * This follows the page's remark that the default (atomic) dq summation is
+   * non-deterministic (constraints section). */
+  int32_t deterministic;
   int64_t wait_timeout_ns; /* bound on every in-kernel wait; <= 0: 2 s */
   /* Optional cudaEvent_t[4] (caller-created, may be NULL): recorded on
    * `stream` before the preprocess kernel, before the main kernel, after the
@@ -137,7 +146,8 @@ fa_status fa_varlen_bwd_workspace_size(
 /* Backward: dq, dk, dv from q, k, v, dy, y (attentionIn) and the forward
  * statistics.  dq, dk, dv are fully overwritten (rows of keys that no query
  * attends to get zeros).  Non-deterministic: dq is summed with fp32 atomics
- * (the constraint section: non-deterministic by default). */
+ * (the constraint section: non-deterministic by default); the options'
+ * deterministic flag of fa_varlen_bwd_ex makes it reproducible. */
 fa_status fa_varlen_bwd(
     const void *q, const void *k, const void *v, const void *dy,
     const uint8_t *drop_mask, int64_t drop_mask_bytes,

@@ -207,3 +207,33 @@ def test_selftest_argument_checks():
     assert L.fa_varlen_selftest_wait_timeout(fake, 64, 10**6, None) == fa.FA_ERR_WORKSPACE
     assert L.fa_varlen_selftest_wait_timeout(fake, 256, 10, None) == fa.FA_ERR_INVALID
     assert L.fa_varlen_selftest_wait_timeout(fake, 256, 10**11, None) == fa.FA_ERR_INVALID
+
+
+@pytest.mark.parametrize("kv_tile", [64, 128])
+@pytest.mark.parametrize("case", SCHED_CASES + [([50, 300], 2, 30, 10), ([700, 1], 1, 0, 0)])
+def test_key_tiles_of_a_query_tile_are_contiguous(case, kv_tile):
+    """The deterministic mode adds the dQ partials of a query tile in key-tile
+    order, ranked from the first key tile that visits it; that needs the key
+    tiles visiting any one query tile to form a contiguous range."""
+    lens, nkv, pre, nxt = case
+    items = fa.bwd_schedule(lens, lens, nkv, pre, nxt, kv_tile)
+    cover = {}
+    for b, h, t, lo, cnt in items:
+        if h != 0:
+            continue
+        for qt in range(lo, lo + cnt):
+            cover.setdefault((b, qt), []).append(t)
+    for key, tiles in cover.items():
+        tiles.sort()
+        assert tiles == list(range(tiles[0], tiles[-1] + 1)), (key, tiles)
+
+
+def test_deterministic_option_accepted():
+    lq = (ctypes.c_int64 * 2)(37, 64)
+    out = ctypes.c_size_t(0)
+    opt = fa.BwdOptions(fa.FA_BWD_AUTO, 1, 0, None)
+    assert fa.lib().fa_varlen_bwd_workspace_size_ex(lq, lq, 2, 101, 101, 2, 2, 64,
+                                                    fa._DTYPE[torch.float32], b"TND", 1.0, BIG,
+                                                    BIG, 0, ctypes.byref(opt),
+                                                    ctypes.byref(out)) == fa.FA_OK
+    assert out.value > 0

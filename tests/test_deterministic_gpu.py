@@ -1,0 +1,84 @@
+"""Deterministic mode: the dQ partials of each (query head, query tile) are
+added in ascending key-tile order, so repeated calls give the same dQ bit for
+bit.  The result must still match the fp64 oracle to the usual tolerance."""
+
+import numpy as np
+import pytest
+import torch
+
+from varlen_flashattention_backward_gb300 import binding as fa
+from varlen_flashattention_backward_gb300 import build as fb
+from varlen_flashattention_backward_gb300 import workloads as wl
+
+from _helpers import TOL, device_mask, f64, oracle_full, rel_err
+
+pytestmark = pytest.mark.gpu
+BIG = wl.UNBOUNDED
+DEV = torch.device("cuda:0")
+IMPLS = {"simt": fa.FA_BWD_SIMT, "tcgen05": fa.FA_BWD_TCGEN05}
+
+CASES = {
+    "w2_causal": wl.workload(2),
+    "ragged_causal": wl.Workload(40, "bf16", [1, 0, 37, 65, 127, 129, 200, 700], 2, 128, BIG,
+                                 0, seed=13),
+    "gqa_band_dropout": wl.Workload(41, "bf16", [300, 0, 450], 4, 128, 100, 20, keep_prob=0.8,
+                                    seed=14, n_heads_kv=2),
+    "lq_ne_lk": wl.Workload(42, "bf16", [50, 300], 2, 128, 30, 10, seed=15, lens_kv=[120, 40]),
+    "fp32_band": wl.Workload(43, "fp32", [170, 45], 2, 64, 20, 3, seed=16),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    fb.build()
+    fa.lib()
+    torch.cuda.set_device(DEV)
+
+
+def _run(w, tensors, mask, impl, deterministic, stats=None):
+    q, k, v, dy = (t.to(DEV) for t in tensors)
+    if stats is None:
+        stats = fa.fwd(q, k, v, w.lens, w.lens_kv, w.scale, w.pre_tokens, w.next_tokens,
+                       w.keep_prob, mask)
+    y, m, l = stats
+    out = fa.bwd(q, k, v, dy, y, m, l, w.lens, w.lens_kv, w.scale, w.pre_tokens,
+                 w.next_tokens, w.keep_prob, mask, impl=impl, deterministic=deterministic)
+    torch.cuda.synchronize()
+    return out, stats
+
+
+@pytest.mark.parametrize("impl", ["simt", "tcgen05"])
+@pytest.mark.parametrize("name", list(CASES))
+def test_deterministic_is_bitwise_repeatable_and_correct(name, impl):
+    w = CASES[name]
+    if impl == "tcgen05" and (w.dtype == "fp32" or w.head_dim != 128):
+        pytest.skip("tcgen05 kernel not built for this case")
+    tensors = wl.make_tensors(w)
+    mask = device_mask(w, DEV)
+    a, stats = _run(w, tensors, mask, IMPLS[impl], True)
+    runs = [_run(w, tensors, mask, IMPLS[impl], True, stats)[0] for _ in range(3)]
+    for r in runs:
+        for x, y in zip(a, r):
+            assert torch.equal(x, y)
+    mask_np = None if mask is None else mask.cpu().numpy()
+    ref = oracle_full(w, tensors, mask_np)
+    tol = TOL[w.dtype]
+    for key, g in zip(("dq", "dk", "dv"), a):
+        assert rel_err(f64(g), ref[key]) <= tol, key
+
+
+@pytest.mark.parametrize("cid", [3, 4, 5])
+def test_deterministic_full_size(cid):
+    """At the benchmark sizes: two deterministic calls agree bit for bit and
+    match the default (atomic) call to well within the tolerance."""
+    w = wl.workload(cid)
+    tensors = wl.make_tensors(w)
+    mask = device_mask(w, DEV)
+    a, stats = _run(w, tensors, mask, fa.FA_BWD_AUTO, True)
+    b, _ = _run(w, tensors, mask, fa.FA_BWD_AUTO, True, stats)
+    c, _ = _run(w, tensors, mask, fa.FA_BWD_AUTO, False, stats)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    for x, y in zip(a, c):
+        den = y.float().abs().max().item()
+        assert (x.float() - y.float()).abs().max().item() <= 1e-2 * den

@@ -119,13 +119,13 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _opts(impl=FA_BWD_AUTO, wait_timeout_ns=0, events=None):
+def _opts(impl=FA_BWD_AUTO, wait_timeout_ns=0, events=None, deterministic=False):
     ev = None
     if events is not None:
         arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
         ev = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
         ev._keep = arr
-    return BwdOptions(int(impl), 0, int(wait_timeout_ns), ev)
+    return BwdOptions(int(impl), int(bool(deterministic)), int(wait_timeout_ns), ev)
 
 
 def fwd_workspace_size(lens_q, lens_kv, n, n_kv, d, dtype, keep_prob=1.0,
@@ -183,9 +183,12 @@ def fwd(q, k, v, lens_q, lens_kv, scale, pre_tokens, next_tokens, keep_prob=1.0,
 
 def bwd(q, k, v, dy, y, softmax_max, softmax_sum, lens_q, lens_kv, scale, pre_tokens,
         next_tokens, keep_prob=1.0, drop_mask=None, dq=None, dk=None, dv=None,
-        workspace=None, stream=None, impl=FA_BWD_AUTO, wait_timeout_ns=0, events=None):
+        workspace=None, stream=None, impl=FA_BWD_AUTO, wait_timeout_ns=0, events=None,
+        deterministic=False):
     """dQ, dK, dV (fa_varlen_bwd_ex).  ``events``: four torch.cuda.Event
-    (already recorded once, so that they exist) recorded around the kernels."""
+    (already recorded once, so that they exist) recorded around the kernels.
+    ``deterministic``: add the dQ partials in a fixed order (bitwise
+    reproducible dQ)."""
     tq, n, d = q.shape
     n_kv = k.shape[1]
     lq, b, _ = _lens(lens_q)
@@ -201,7 +204,7 @@ def bwd(q, k, v, dy, y, softmax_max, softmax_sum, lens_q, lens_kv, scale, pre_to
                                 next_tokens, impl)
         workspace = torch.empty(ws, dtype=torch.uint8, device=q.device)
     mask_bytes = 0 if drop_mask is None else drop_mask.numel()
-    opt = _opts(impl, wait_timeout_ns, events)
+    opt = _opts(impl, wait_timeout_ns, events, deterministic)
     _check(lib().fa_varlen_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(dy), _ptr(drop_mask),
                                   mask_bytes, _ptr(softmax_max), _ptr(softmax_sum), _ptr(y), lq,
                                   lk, b, tq, k.shape[0], n, n_kv, d, _DTYPE[q.dtype], b"TND",

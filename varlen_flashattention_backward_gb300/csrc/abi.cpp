@@ -106,7 +106,11 @@ std::vector<SeqInfo> build_seqs(const Problem &pr) {
 // in flight at any moment stay few: their Q, dY and dQ accumulator rows
 // (about 1 MB each per 2048 tokens) stay resident in L2 across the key
 // tiles that re-read them.
-std::vector<WorkItem> build_bwd_items(const Problem &pr, int kv_tile) {
+//
+// In the deterministic mode the items of a unit stay in ascending key-tile
+// order instead, so that a CTA only ever waits for items taken before its own
+// (see BwdParams::deterministic).
+std::vector<WorkItem> build_bwd_items(const Problem &pr, int kv_tile, bool tile_order) {
   struct Unit {
     size_t first, count;
     int max_len;
@@ -130,10 +134,11 @@ std::vector<WorkItem> build_bwd_items(const Problem &pr, int kv_tile) {
         items.push_back({int32_t(b), int32_t(h), int32_t(t), int32_t(qlo | (cnt << 16))});
         u.max_len = std::max(u.max_len, int(cnt));
       }
-      std::stable_sort(items.begin() + u.first, items.end(),
-                       [](const WorkItem &a, const WorkItem &c) {
-                         return item_count(a) > item_count(c);
-                       });
+      if (!tile_order)
+        std::stable_sort(items.begin() + u.first, items.end(),
+                         [](const WorkItem &a, const WorkItem &c) {
+                           return item_count(a) > item_count(c);
+                         });
       if (tiles > 0) units.push_back(u);
     }
   }
@@ -179,8 +184,34 @@ int64_t count_items(const Problem &pr, int tile, bool fwd) {
   return c;
 }
 
+// First key tile visiting each padded query tile (the deterministic mode's
+// order base).  The key tiles that visit one query tile form a contiguous
+// range for every window, because both ends of a key tile's query range grow
+// with the tile index; the check below guards that property.
+bool build_qfirst(const Problem &pr, const std::vector<SeqInfo> &seqs,
+                  const std::vector<WorkItem> &items, std::vector<int32_t> &qfirst) {
+  const size_t g_tiles = size_t(pr.tp / kQTile);
+  std::vector<int32_t> lo(g_tiles, INT32_MAX), hi(g_tiles, -1), cnt(g_tiles, 0);
+  for (const WorkItem &w : items) {
+    if (w.head != 0) continue;
+    const size_t g0 = size_t(seqs[size_t(w.seq)].qpad / kQTile) + size_t(item_lo(w));
+    for (int t = 0; t < item_count(w); ++t) {
+      lo[g0 + t] = std::min(lo[g0 + t], w.tile);
+      hi[g0 + t] = std::max(hi[g0 + t], w.tile);
+      ++cnt[g0 + t];
+    }
+  }
+  qfirst.assign(g_tiles, 0);
+  for (size_t g = 0; g < g_tiles; ++g) {
+    if (cnt[g] == 0) continue;
+    if (hi[g] - lo[g] + 1 != cnt[g]) return false;
+    qfirst[g] = lo[g];
+  }
+  return true;
+}
+
 struct BwdLayout {
-  size_t seqs, items, lse, dsum, dqacc, total;
+  size_t seqs, items, qfirst, lse, dsum, sem, dqacc, total;
 };
 
 int choose_bwd_impl(const Problem &pr, const fa_bwd_options *opt) {
@@ -201,10 +232,14 @@ BwdLayout bwd_layout(const Problem &pr, int impl) {
   off = align_up(off + sizeof(SeqInfo) * size_t(pr.batch));
   L.items = off;
   off = align_up(off + sizeof(WorkItem) * size_t(count_items(pr, tile, false)));
+  L.qfirst = off;
+  off = align_up(off + sizeof(int32_t) * size_t(pr.tp / kQTile));
   L.lse = off;
   off = align_up(off + sizeof(float) * size_t(pr.n * pr.tp));
   L.dsum = off;
   off = align_up(off + sizeof(float) * size_t(pr.n * pr.tp));
+  L.sem = off;
+  off = align_up(off + sizeof(int32_t) * size_t(pr.n * (pr.tp / kQTile)));
   L.dqacc = off;
   off = align_up(off + sizeof(float) * size_t(pr.total_q * pr.n * pr.d));
   L.total = off;
@@ -220,15 +255,20 @@ size_t fwd_layout_total(const Problem &pr, size_t *seqs_off, size_t *items_off) 
   return off;
 }
 
-// Uploads [header | seqs | items] with one copy; the header's error word is 0.
+// Uploads [header | seqs | items | table] with one copy; the header's error
+// word and ticket are 0.
 fa_status upload_plan(void *ws, size_t seqs_off, size_t items_off,
                       const std::vector<SeqInfo> &seqs, const std::vector<WorkItem> &items,
-                      cudaStream_t st) {
-  const size_t bytes = items_off + sizeof(WorkItem) * items.size();
+                      cudaStream_t st, size_t table_off = 0,
+                      const std::vector<int32_t> *table = nullptr) {
+  size_t bytes = items_off + sizeof(WorkItem) * items.size();
+  if (table && !table->empty()) bytes = table_off + sizeof(int32_t) * table->size();
   std::vector<uint8_t> host(bytes, 0);
   std::memcpy(host.data() + seqs_off, seqs.data(), sizeof(SeqInfo) * seqs.size());
   if (!items.empty())
     std::memcpy(host.data() + items_off, items.data(), sizeof(WorkItem) * items.size());
+  if (table && !table->empty())
+    std::memcpy(host.data() + table_off, table->data(), sizeof(int32_t) * table->size());
   if (cudaMemcpyAsync(ws, host.data(), bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
     return FA_ERR_CUDA;
   return FA_OK;
@@ -341,8 +381,7 @@ fa_status fa_varlen_bwd_workspace_size_ex(const int64_t *seq_lens_q, const int64
              head_dim, dtype, keep_prob, pre_tokens, next_tokens, sparse_mode, 0, 0};
   fa_status st = check_problem(pr, layout, {});
   if (st != FA_OK) return st;
-  if (options && (options->deterministic != 0 || options->impl < FA_BWD_AUTO ||
-                  options->impl > FA_BWD_TCGEN05))
+  if (options && (options->impl < FA_BWD_AUTO || options->impl > FA_BWD_TCGEN05))
     return FA_ERR_INVALID;
   const int impl = choose_bwd_impl(pr, options);
   if (impl == FA_BWD_TCGEN05 && !tcgen05_supported(dtype, int(head_dim)))
@@ -389,8 +428,7 @@ fa_status fa_varlen_bwd_ex(const void *q, const void *k, const void *v, const vo
   if (dropout && drop_mask == nullptr) return FA_ERR_NULLPTR;
   if (!std::isfinite(scale)) return FA_ERR_INVALID;
   if (dropout && drop_mask_bytes < (pr.mask_bits + 7) / 8) return FA_ERR_INVALID;
-  if (options && (options->deterministic != 0 || options->impl < FA_BWD_AUTO ||
-                  options->impl > FA_BWD_TCGEN05))
+  if (options && (options->impl < FA_BWD_AUTO || options->impl > FA_BWD_TCGEN05))
     return FA_ERR_INVALID;
   int impl = choose_bwd_impl(pr, options);
   if (impl == FA_BWD_TCGEN05 && !tcgen05_supported(dtype, int(head_dim)))
@@ -410,9 +448,12 @@ fa_status fa_varlen_bwd_ex(const void *q, const void *k, const void *v, const vo
 
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const int tile = impl == FA_BWD_TCGEN05 ? kTcKvTile : kSimtKvTile;
+  const bool det = options && options->deterministic != 0;
   auto seqs = build_seqs(pr);
-  auto items = build_bwd_items(pr, tile);
-  st = upload_plan(workspace, L.seqs, L.items, seqs, items, cs);
+  auto items = build_bwd_items(pr, tile, det);
+  std::vector<int32_t> qfirst;
+  if (det && !build_qfirst(pr, seqs, items, qfirst)) return FA_ERR_UNSUPPORTED;
+  st = upload_plan(workspace, L.seqs, L.items, seqs, items, cs, L.qfirst, det ? &qfirst : nullptr);
   if (st != FA_OK) return st;
 
   uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -427,6 +468,10 @@ fa_status fa_varlen_bwd_ex(const void *q, const void *k, const void *v, const vo
   p.dsum = reinterpret_cast<float *>(ws + L.dsum);
   p.dq_acc = reinterpret_cast<float *>(ws + L.dqacc);
   p.err = reinterpret_cast<int32_t *>(ws);
+  p.deterministic = det ? 1 : 0;
+  p.ticket = reinterpret_cast<int32_t *>(ws + kTicketOffset);
+  p.sem = reinterpret_cast<int32_t *>(ws + L.sem);
+  p.qfirst = reinterpret_cast<const int32_t *>(ws + L.qfirst);
   p.n_items = int(items.size());
   p.batch = int(batch); p.n = int(head_num); p.n_kv = int(head_num_kv); p.d = int(head_dim);
   p.tp = int(pr.tp); p.total_q = int(total_q); p.total_kv = int(total_kv);
@@ -444,6 +489,10 @@ fa_status fa_varlen_bwd_ex(const void *q, const void *k, const void *v, const vo
            cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), cs) == cudaSuccess;
   };
   if (!mark(0)) return FA_ERR_CUDA;
+  if (det && pr.tp > 0 &&
+      cudaMemsetAsync(p.sem, 0, sizeof(int32_t) * size_t(pr.n * (pr.tp / kQTile)), cs) !=
+          cudaSuccess)
+    return FA_ERR_CUDA;
   if (pr.tp > 0 && launch_bwd_preprocess(p, dtype, cs) != cudaSuccess) return FA_ERR_CUDA;
   if (!mark(1)) return FA_ERR_CUDA;
   if (!items.empty()) {
@@ -501,7 +550,7 @@ fa_status fa_varlen_bwd_schedule(const int64_t *seq_lens_q, const int64_t *seq_l
       return FA_ERR_INVALID;
   Problem pr{seq_lens_q, seq_lens_kv, batch, 0, 0, head_num_kv, head_num_kv, 128,
              FA_DTYPE_BF16, 1.0, pre_tokens, next_tokens, 0, 0, 0};
-  auto list = build_bwd_items(pr, kv_tile);
+  auto list = build_bwd_items(pr, kv_tile, false);
   *n_items = int64_t(list.size());
   const int64_t m = std::min<int64_t>(capacity, int64_t(list.size()));
   if (m > 0) std::memcpy(items, list.data(), size_t(m) * sizeof(WorkItem));

@@ -159,6 +159,11 @@ __device__ __forceinline__ void st_global_v4(void *ptr, uint32_t a, uint32_t b, 
                : "memory");
 }
 
+// Named barrier 1 joins the four dQ drain warps (warps 12-15).
+__device__ __forceinline__ void drain_bar_sync() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
 struct Ctl {
   int *abort;         // shared-memory flag: some wait of this CTA gave up
   int32_t *err;       // global error word
@@ -184,16 +189,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t sb = smem_u32(sm);
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ int s_item;
+  __shared__ int s_dq_ok;
   auto bar = [&](int i) { return sb + SM_BAR + 8u * uint32_t(i); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const WorkItem item = p.items[blockIdx.x];
-  const SeqInfo sq = p.seqs[item.seq];
-  const int kvh = item.head;
-  const int group = p.n / p.n_kv;
-  const int k0 = item.tile * BN;
-  const int qlo = item_lo(item), qcnt = item_count(item);
-  const int n_it = qcnt * group;
   Ctl ctl{&s_abort, p.err, p.timeout_ns};
   // Waits for this CTA's own copies and MMAs in flight (which finish without
   // help from any other role) are bounded by at least a second, whatever
@@ -202,6 +202,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (threadIdx.x == 0) {
     s_abort = 0;
+    s_item = take_item(p);
     mbar_init(bar(B_KV), 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar(B_FULL + s), 1);
@@ -229,6 +230,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
+  const WorkItem item = p.items[s_item];
+  const SeqInfo sq = p.seqs[item.seq];
+  const int kvh = item.head;
+  const int group = p.n / p.n_kv;
+  const int k0 = item.tile * BN;
+  const int qlo = item_lo(item), qcnt = item_count(item);
+  const int n_it = qcnt * group;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -526,6 +534,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tmem_ld32(tmem + lane_off + COL_DQ + 32, b);
       tc_fence_before();
       if (lane == 0) mbar_arrive(bar(B_DQFREE));
+      // Deterministic mode: wait until the key tiles before this one have
+      // added their partials of this query tile (the counter holds how many
+      // have), add, then publish count + 1.
+      int32_t *ctr = nullptr;
+      int rank = 0;
+      if (p.deterministic) {
+        const int qt = qlo + L % qcnt;
+        ctr = dq_counter(p, sq, n, qt);
+        rank = dq_rank(p, sq, item.tile, qt);
+        if (warp == 12 && lane == 0) {
+          const bool got = wait_counter(ctr, rank, p.timeout_ns,
+                                        reinterpret_cast<volatile int *>(&s_abort));
+          if (!got && !*reinterpret_cast<volatile int *>(&s_abort)) {
+            atomicExch(&s_abort, 1);
+            atomicCAS(p.err, 0, kErrTimeoutBase + ROLE_DQ);
+          }
+          s_dq_ok = got ? 1 : 0;
+        }
+        drain_bar_sync();
+        if (!*reinterpret_cast<volatile int *>(&s_dq_ok)) break;
+      }
       // Thread (quad m, c) holds column d = quarter*32 + 4m + c for 64 queries.
       // A 4 x 4 transpose inside each quad (two xor-shuffle rounds) gives it
       // d = quarter*32 + 4m + 0..3 at query 4j + c, so that each reduction
@@ -549,6 +578,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const float u1 = __shfl_xor_sync(0xffffffffu, hi1 ? r2 : r3, 1);
         if (4 * j + c < rows)
           red_add_v4_f32(ptr, hi1 ? u0 : r0, hi1 ? r1 : u0, hi1 ? u1 : r2, hi1 ? r3 : u1);
+      }
+      if (p.deterministic) {
+        __threadfence();
+        drain_bar_sync();
+        if (warp == 12 && lane == 0) st_release_gpu(ctr, rank + 1);
       }
     }
   }

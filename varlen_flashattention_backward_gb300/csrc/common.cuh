@@ -46,4 +46,54 @@ __device__ __forceinline__ int seq_of_padded_row(const SeqInfo *seqs, int batch,
   return lo;
 }
 
+// ---------------------------------------------------------------------------
+// Ordered dQ adds of the deterministic mode (BwdParams::deterministic).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t *ptr) {
+  int32_t v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(int32_t *ptr, int32_t v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ long long timer_ns() {
+  long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Spins until *ptr == want.  Gives up (false) once timeout_ns has passed or,
+// when `abort` is non-null, once *abort is set.
+__device__ __forceinline__ bool wait_counter(const int32_t *ptr, int32_t want, long long timeout_ns,
+                                             const volatile int *abort) {
+  if (ld_acquire_gpu(ptr) == want) return true;
+  const long long t0 = timer_ns();
+  while (true) {
+    __nanosleep(100);
+    if (ld_acquire_gpu(ptr) == want) return true;
+    if (abort != nullptr && *abort) return false;
+    if (timer_ns() - t0 > timeout_ns) return false;
+  }
+}
+
+// Item index of this CTA: its grid index, or in the deterministic mode the
+// next ticket, so that items are taken in list order by CTAs that are already
+// running.  Call from one thread.
+__device__ __forceinline__ int take_item(const BwdParams &p) {
+  return p.deterministic ? atomicAdd(p.ticket, 1) : int(blockIdx.x);
+}
+
+// Counter and rank of the dQ partial that key tile `tile` adds to query tile
+// `qt` (0-based inside the sequence) of query head n.
+__device__ __forceinline__ int32_t *dq_counter(const BwdParams &p, const SeqInfo &s, int n,
+                                               int qt) {
+  return p.sem + int64_t(n) * (p.tp / kQTile) + s.qpad / kQTile + qt;
+}
+__device__ __forceinline__ int dq_rank(const BwdParams &p, const SeqInfo &s, int tile, int qt) {
+  return tile - p.qfirst[s.qpad / kQTile + qt];
+}
+
 }  // namespace fav

@@ -42,7 +42,12 @@ __host__ __device__ inline int item_count(const WorkItem &w) { return (w.range >
 enum : int32_t {
   kErrNone = 0,
   kErrTimeoutBase = 0x100,   // + role id of the wait that expired
+  kRoleSimtDq = 8,           // the CUDA-core backward's ordered dQ wait
 };
+
+// Workspace header (kHeaderBytes): the error word at byte 0 and, in the
+// deterministic mode, the work-item ticket counter at byte kTicketOffset.
+constexpr size_t kTicketOffset = 64;
 
 struct BwdParams {
   const void *q, *k, *v, *dy, *y;
@@ -56,6 +61,14 @@ struct BwdParams {
   float *dsum;      // [N][Tp]  sum_d dY * Y;               0 for padding rows
   float *dq_acc;    // [Tq][N][D] fp32 accumulator of dS K (unscaled)
   int32_t *err;
+  // Deterministic mode: CTAs take items in ticket order (*ticket counts up
+  // from 0) and add their dQ partials of (query head n, padded query tile g)
+  // in ascending key-tile order.  sem[n * (tp / 64) + g] counts the partials
+  // already added; qfirst[g] is the first key tile that visits tile g.
+  int deterministic;
+  int32_t *ticket;
+  int32_t *sem;
+  const int32_t *qfirst;
   int n_items, batch, n, n_kv, d, tp, total_q, total_kv;
   int pre, next;    // clamped to +-2^30
   float scale, scale_log2, inv_keep;

@@ -172,7 +172,10 @@ __global__ void __launch_bounds__(256) bwd_simt_kernel(BwdParams p) {
   float *lse_s = dSs + 64 * PD;
   float *dsum_s = lse_s + 64;
 
-  const WorkItem it = p.items[blockIdx.x];
+  __shared__ int s_item, s_ok;
+  if (threadIdx.x == 0) s_item = take_item(p);
+  __syncthreads();
+  const WorkItem it = p.items[s_item];
   const SeqInfo s = p.seqs[it.seq];
   const int kvh = it.head;
   const int group = p.n / p.n_kv;
@@ -309,6 +312,20 @@ __global__ void __launch_bounds__(256) bwd_simt_kernel(BwdParams p) {
 #pragma unroll
           for (int c = 0; c < DC; ++c) dq[a][c] = fmaf(sv[a], kv[c], dq[a][c]);
       }
+      // Deterministic mode: add after the key tiles before this one, in
+      // ascending order, then let the next one in.
+      int32_t *ctr = nullptr;
+      int rank = 0;
+      if (p.deterministic) {
+        ctr = dq_counter(p, s, n, qt);
+        rank = dq_rank(p, s, it.tile, qt);
+        if (tid == 0) s_ok = wait_counter(ctr, rank, p.timeout_ns, nullptr);
+        __syncthreads();
+        if (!s_ok) {
+          if (tid == 0) atomicCAS(p.err, 0, kErrTimeoutBase + kRoleSimtDq);
+          return;
+        }
+      }
 #pragma unroll
       for (int a = 0; a < 4; ++a) {
         const int gi = q0 + ty + 16 * a;
@@ -317,6 +334,11 @@ __global__ void __launch_bounds__(256) bwd_simt_kernel(BwdParams p) {
 #pragma unroll
           for (int c = 0; c < DC; ++c) atomicAdd(row + tx + 16 * c, dq[a][c]);
         }
+      }
+      if (p.deterministic) {
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) st_release_gpu(ctr, rank + 1);
       }
     }
   }
