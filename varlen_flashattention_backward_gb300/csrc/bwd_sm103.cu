@@ -180,7 +180,9 @@ __device__ __forceinline__ bool wait_or_abort(const Ctl &c, uint32_t bar, uint32
   return false;
 }
 
-template <bool kBF16>
+// kDet: the deterministic mode (ticket-ordered items, ordered dQ adds); a
+// separate instantiation so that the default kernel carries none of it.
+template <bool kBF16, bool kDet>
 __global__ void __launch_bounds__(NTHREADS, 1)
     bwd_tc_kernel(const BwdParams p, const __grid_constant__ TcMaps maps) {
   extern __shared__ uint8_t smem_raw[];
@@ -194,6 +196,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   auto bar = [&](int i) { return sb + SM_BAR + 8u * uint32_t(i); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  WorkItem item_by_grid{};
+  if (!kDet) item_by_grid = p.items[blockIdx.x];
   Ctl ctl{&s_abort, p.err, p.timeout_ns};
   // Waits for this CTA's own copies and MMAs in flight (which finish without
   // help from any other role) are bounded by at least a second, whatever
@@ -202,7 +206,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (threadIdx.x == 0) {
     s_abort = 0;
-    s_item = take_item(p);
+    if (kDet) s_item = atomicAdd(p.ticket, 1);
     mbar_init(bar(B_KV), 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar(B_FULL + s), 1);
@@ -230,7 +234,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  const WorkItem item = p.items[s_item];
+  const WorkItem item = kDet ? p.items[s_item] : item_by_grid;
   const SeqInfo sq = p.seqs[item.seq];
   const int kvh = item.head;
   const int group = p.n / p.n_kv;
@@ -539,7 +543,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // have), add, then publish count + 1.
       int32_t *ctr = nullptr;
       int rank = 0;
-      if (p.deterministic) {
+      if constexpr (kDet) {
         const int qt = qlo + L % qcnt;
         ctr = dq_counter(p, sq, n, qt);
         rank = dq_rank(p, sq, item.tile, qt);
@@ -579,7 +583,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (4 * j + c < rows)
           red_add_v4_f32(ptr, hi1 ? u0 : r0, hi1 ? r1 : u0, hi1 ? u1 : r2, hi1 ? r3 : u1);
       }
-      if (p.deterministic) {
+      if constexpr (kDet) {
         __threadfence();
         drain_bar_sync();
         if (warp == 12 && lane == 0) st_release_gpu(ctr, rank + 1);
@@ -650,7 +654,7 @@ bool make_map(CUtensorMap *m, const void *base, int64_t rows, int heads, int box
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kBF16>
+template <bool kBF16, bool kDet>
 cudaError_t launch_t(const BwdParams &p, cudaStream_t st) {
   TcMaps maps;
   if (!make_map(&maps.q, p.q, p.total_q, p.n, BM, kBF16) ||
@@ -658,10 +662,10 @@ cudaError_t launch_t(const BwdParams &p, cudaStream_t st) {
       !make_map(&maps.k, p.k, p.total_kv, p.n_kv, BN, kBF16) ||
       !make_map(&maps.v, p.v, p.total_kv, p.n_kv, BN, kBF16))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<kBF16>,
+  cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<kBF16, kDet>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  bwd_tc_kernel<kBF16><<<p.n_items, NTHREADS, SMEM_BYTES, st>>>(p, maps);
+  bwd_tc_kernel<kBF16, kDet><<<p.n_items, NTHREADS, SMEM_BYTES, st>>>(p, maps);
   return cudaGetLastError();
 }
 
@@ -679,8 +683,8 @@ bool tcgen05_supported(fa_dtype dt, int head_dim) {
 }
 
 cudaError_t launch_bwd_tcgen05(const BwdParams &p, fa_dtype dt, cudaStream_t s) {
-  if (dt == FA_DTYPE_BF16) return launch_t<true>(p, s);
-  if (dt == FA_DTYPE_FP16) return launch_t<false>(p, s);
+  if (dt == FA_DTYPE_BF16) return p.deterministic ? launch_t<true, true>(p, s) : launch_t<true, false>(p, s);
+  if (dt == FA_DTYPE_FP16) return p.deterministic ? launch_t<false, true>(p, s) : launch_t<false, false>(p, s);
   return cudaErrorInvalidValue;
 }
 
