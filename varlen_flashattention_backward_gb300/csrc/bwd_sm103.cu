@@ -78,12 +78,13 @@ constexpr uint32_t SM_DSUM = SM_LSE + STAGES * 256;
 constexpr uint32_t SM_BAR = SM_DSUM + STAGES * 256;
 constexpr uint32_t SM_TOTAL = SM_BAR + 256;
 constexpr uint32_t SMEM_BYTES = SM_TOTAL + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 
 // mbarrier slots
 enum : int {
-  B_KV = 0, B_FULL = 1, B_EMPTY = B_FULL + STAGES, B_SFULL = B_EMPTY + STAGES, B_SFREE,
-  B_DPFULL, B_DPFREE, B_PFULL, B_PFREE, B_DSFULL, B_DSFREE, B_DQFULL, B_DQFREE, B_ACC,
-  B_FINAL, B_COUNT
+  B_KV = 0, B_FULL = 1, B_EMPTY = B_FULL + STAGES, B_SDFULL = B_EMPTY + STAGES, B_SDFREE,
+  B_PFULL, B_PFREE, B_DSFULL, B_DSFREE, B_DQFULL, B_DQFREE, B_ACC, B_FINAL, B_FINAL_A,
+  B_COUNT
 };
 static_assert(B_COUNT * 8 <= 256, "barrier area");
 
@@ -212,10 +213,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(bar(B_FULL + s), 1);
       mbar_init(bar(B_EMPTY + s), 1);
     }
-    mbar_init(bar(B_SFULL), 1);
-    mbar_init(bar(B_SFREE), 8);
-    mbar_init(bar(B_DPFULL), 1);
-    mbar_init(bar(B_DPFREE), 8);
+    mbar_init(bar(B_SDFULL), 1);
+    mbar_init(bar(B_SDFREE), 8);
     mbar_init(bar(B_PFULL), 8);
     mbar_init(bar(B_PFREE), 1);
     mbar_init(bar(B_DSFULL), 8);
@@ -224,6 +223,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(bar(B_DQFREE), 4);
     mbar_init(bar(B_ACC), 1);
     mbar_init(bar(B_FINAL), 1);
+    mbar_init(bar(B_FINAL_A), 1);
     mbar_fence_init();
   }
   if (warp == 1) {
@@ -285,10 +285,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int L = issued > STAGES ? issued - STAGES : 0; L < issued; ++L)
         mbar_wait(bar(B_FULL + L % STAGES), (L / STAGES) & 1, drain_ns, &never);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs this loop; each MMA and commit is issued by one
-    // elected lane from straight-line code (see mma_ss_w).
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two warps issue the tensor-core work, so that two independent chains
+    // of dependent MMAs are in flight at once (one issuing warp cannot keep
+    // the tensor core busy with 36 small MMAs per tile):
+    //   warp 1:  S^T = K Q^T and dP^T = V dY^T of tile L, interleaved;
+    //   warp 2:  dV += P^T dY, then dK += dS^T Q interleaved with dQ^T.
+    // A commit tracks the MMAs of the thread that issues it, so each warp
+    // signals only its own work.  Each warp issues from straight-line code,
+    // one elected lane per MMA (see mma_ss_w).
     if (n_it > 0) {
       const uint32_t id_s = idesc_f16(128, BM, false, false, kBF16);   // S^T, dP^T
       const uint32_t id_g = idesc_f16(128, HD, false, true, kBF16);    // dV, dK
@@ -300,76 +306,74 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint64_t dv_ = sdesc_sw128(sb + SM_V, 16, 1024);     // V, K-major
       const uint64_t dkt = sdesc_sw128(sb + SM_K, 16384, 1024);  // K, MN-major (K^T)
       const uint64_t dds = sdesc_sw128(sb + SM_DS, 16384, 1024); // dS^T, MN-major
-      auto mma_kt = [&](uint64_t a0, uint32_t b_base, uint32_t dcol) {
-        // D[128 x 64] = A[128 x 128] B[64 x 128]^T, both K-major (2 boxes along K)
-        const uint64_t b0 = sdesc_sw128(b_base, 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk & 3) * 32;
-          mma_ss_w(tmem + dcol, a0 + (((kk >> 2) * 16384 + off) >> 4),
-                   b0 + (((kk >> 2) * 8192 + off) >> 4), id_s, kk > 0 ? 1u : 0u);
-        }
-      };
-      auto mma_grad = [&](uint32_t a_col, uint32_t b_base, uint32_t dcol, uint32_t acc) {
-        // D[128 x 128] += A[128 x 64] (TMEM) B[64 x 128] (MN-major)
-        const uint64_t b0 = sdesc_sw128(b_base, 8192, 1024);
-        mma_ts_w(tmem + dcol, tmem + a_col, b0, id_g, acc);
-#pragma unroll
-        for (int kk = 1; kk < BM / 16; ++kk)
-          mma_ts_w(tmem + dcol, tmem + a_col + kk * 8, b0 + ((kk * 2048) >> 4), id_g, 1u);
-      };
-      auto mma_dq = [&]() {
-        // dQ^T[128 d x 64 q] = K^T[128 d x 128 keys] dS^T[128 keys x 64 q]
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ss_w(tmem + COL_DQ, dkt + ((kk * 2048) >> 4), dds + ((kk * 2048) >> 4), id_q,
-                   kk > 0 ? 1u : 0u);
-      };
-      bool ok = wait_or_abort(ctl, bar(B_KV), 0, ROLE_MMA) &&
-                wait_or_abort(ctl, bar(B_FULL), 0, ROLE_MMA);
-      tc_fence_after();
-      if (ok) {
-        mma_kt(dk_, sb + SM_Q, COL_S);
-        mma_commit_w(bar(B_SFULL));
-        mma_kt(dv_, sb + SM_DY, COL_DP);
-        mma_commit_w(bar(B_DPFULL));
-      }
-      for (int L = 0; ok && L < n_it; ++L) {
-        const int st = L % STAGES;
-        if (L + 1 < n_it) {
-          const int s1 = (L + 1) % STAGES;
-          ok = wait_or_abort(ctl, bar(B_FULL + s1), ((L + 1) / STAGES) & 1, ROLE_MMA) &&
-               wait_or_abort(ctl, bar(B_SFREE), L & 1, ROLE_MMA);
+      if (warp == 1) {
+        bool ok = wait_or_abort(ctl, bar(B_KV), 0, ROLE_MMA);
+        for (int L = 0; ok && L < n_it; ++L) {
+          const int st = L % STAGES;
+          ok = wait_or_abort(ctl, bar(B_FULL + st), (L / STAGES) & 1, ROLE_MMA) &&
+               (L == 0 || wait_or_abort(ctl, bar(B_SDFREE), (L - 1) & 1, ROLE_MMA));
           if (!ok) break;
           tc_fence_after();
-          mma_kt(dk_, sb + SM_Q + s1 * 16384, COL_S);
-          mma_commit_w(bar(B_SFULL));
+          // D[128 x 64] = A[128 x 128] B[64 x 128]^T, both K-major (2 boxes along K)
+          const uint64_t bq = sdesc_sw128(sb + SM_Q + st * 16384, 16, 1024);
+          const uint64_t by = sdesc_sw128(sb + SM_DY + st * 16384, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            const uint32_t ao = (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+            const uint32_t bo = (((kk >> 2) * 8192 + (kk & 3) * 32) >> 4);
+            const uint32_t acc = kk > 0 ? 1u : 0u;
+            mma_ss_w(tmem + COL_S, dk_ + ao, bq + bo, id_s, acc);
+            mma_ss_w(tmem + COL_DP, dv_ + ao, by + bo, id_s, acc);
+          }
+          mma_commit_w(bar(B_SDFULL));
         }
-        if (!(ok = wait_or_abort(ctl, bar(B_PFULL), L & 1, ROLE_MMA))) break;
-        tc_fence_after();
-        mma_grad(COL_P, sb + SM_DY + st * 16384, COL_DV, L > 0 ? 1u : 0u);
-        mma_commit_w(bar(B_PFREE));
-        if (!(ok = wait_or_abort(ctl, bar(B_DSFULL), L & 1, ROLE_MMA))) break;
-        tc_fence_after();
-        mma_grad(COL_DS, sb + SM_Q + st * 16384, COL_DK, L > 0 ? 1u : 0u);
-        if (L > 0 && !(ok = wait_or_abort(ctl, bar(B_DQFREE), (L - 1) & 1, ROLE_MMA))) break;
-        tc_fence_after();
-        mma_dq();
-        mma_commit_w(bar(B_DQFULL));
-        mma_commit_w(bar(B_DSFREE));
-        mma_commit_w(bar(B_EMPTY + st));
-        if (L + 1 < n_it) {
-          if (!(ok = wait_or_abort(ctl, bar(B_DPFREE), L & 1, ROLE_MMA))) break;
+        // Every MMA of this warp has finished before TMEM is freed.
+        mma_commit_w(bar(B_FINAL_A));
+        const int never = 0;
+        mbar_wait(bar(B_FINAL_A), 0, drain_ns, &never);
+      } else {
+        bool ok = wait_or_abort(ctl, bar(B_KV), 0, ROLE_MMA);
+        for (int L = 0; ok && L < n_it; ++L) {
+          const int st = L % STAGES;
+          const uint32_t acc0 = L > 0 ? 1u : 0u;
+          if (!(ok = wait_or_abort(ctl, bar(B_PFULL), L & 1, ROLE_MMA))) break;
           tc_fence_after();
-          mma_kt(dv_, sb + SM_DY + ((L + 1) % STAGES) * 16384, COL_DP);
-          mma_commit_w(bar(B_DPFULL));
+          {
+            // dV[128 x 128] += P^T[128 x 64] (TMEM) dY[64 x 128] (MN-major)
+            const uint64_t b0 = sdesc_sw128(sb + SM_DY + st * 16384, 8192, 1024);
+#pragma unroll
+            for (int kk = 0; kk < BM / 16; ++kk)
+              mma_ts_w(tmem + COL_DV, tmem + COL_P + kk * 8, b0 + ((kk * 2048) >> 4), id_g,
+                       kk > 0 ? 1u : acc0);
+          }
+          mma_commit_w(bar(B_PFREE));
+          if (!(ok = wait_or_abort(ctl, bar(B_DSFULL), L & 1, ROLE_MMA))) break;
+          if (L > 0 && !(ok = wait_or_abort(ctl, bar(B_DQFREE), (L - 1) & 1, ROLE_MMA))) break;
+          tc_fence_after();
+          {
+            // dK[128 x 128] += dS^T[128 x 64] (TMEM) Q[64 x 128] (MN-major), and
+            // dQ^T[128 d x 64 q] = K^T[128 d x 128 keys] dS^T[128 keys x 64 q]
+            const uint64_t b0 = sdesc_sw128(sb + SM_Q + st * 16384, 8192, 1024);
+#pragma unroll
+            for (int kk = 0; kk < BM / 16; ++kk) {
+              mma_ts_w(tmem + COL_DK, tmem + COL_DS + kk * 8, b0 + ((kk * 2048) >> 4), id_g,
+                       kk > 0 ? 1u : acc0);
+              mma_ss_w(tmem + COL_DQ, dkt + (((2 * kk) * 2048) >> 4),
+                       dds + (((2 * kk) * 2048) >> 4), id_q, kk > 0 ? 1u : 0u);
+              mma_ss_w(tmem + COL_DQ, dkt + (((2 * kk + 1) * 2048) >> 4),
+                       dds + (((2 * kk + 1) * 2048) >> 4), id_q, 1u);
+            }
+          }
+          mma_commit_w(bar(B_DQFULL));
+          mma_commit_w(bar(B_DSFREE));
+          mma_commit_w(bar(B_EMPTY + st));
         }
+        if (ok) mma_commit_w(bar(B_ACC));
+        // Every MMA of this warp has finished before TMEM is freed.
+        mma_commit_w(bar(B_FINAL));
+        const int never = 0;
+        mbar_wait(bar(B_FINAL), 0, drain_ns, &never);
       }
-      if (ok) mma_commit_w(bar(B_ACC));
-      // Every MMA of this CTA has finished before TMEM is freed.
-      mma_commit_w(bar(B_FINAL));
-      const int never = 0;
-      mbar_wait(bar(B_FINAL), 0, drain_ns, &never);
     }
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ softmax / dS
@@ -384,13 +388,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int n = kvh * group + L / qcnt;
       const int q0 = (qlo + L % qcnt) * BM;
       const int i0 = q0 + 32 * half;
-      uint32_t r[32];
+      uint32_t r[32], rdp[32];
       float pr[32];
-      if (!wait_or_abort(ctl, bar(B_SFULL), L & 1, ROLE_SOFTMAX)) break;
+      if (!wait_or_abort(ctl, bar(B_SDFULL), L & 1, ROLE_SOFTMAX)) break;
       tc_fence_after();
-      tmem_ld32(tmem + lane_off + COL_S + 32 * half, r);
+      tmem_ld32x2(tmem + lane_off + COL_S + 32 * half, r, tmem + lane_off + COL_DP + 32 * half,
+                  rdp);
       tc_fence_before();
-      if (lane == 0) mbar_arrive(bar(B_SFREE));
+      if (lane == 0) mbar_arrive(bar(B_SDFREE));
       {
         const uint32_t lse_addr = sb + SM_LSE + st * 256 + 128 * half;
 #pragma unroll
@@ -446,11 +451,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_PFULL));
 
-      if (!wait_or_abort(ctl, bar(B_DPFULL), L & 1, ROLE_SOFTMAX)) break;
-      tc_fence_after();
-      tmem_ld32(tmem + lane_off + COL_DP + 32 * half, r);
-      tc_fence_before();
-      if (lane == 0) mbar_arrive(bar(B_DPFREE));
       {
         const uint32_t dsum_addr = sb + SM_DSUM + st * 256 + 128 * half;
 #pragma unroll
@@ -463,11 +463,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int e = 0; e < 4; ++e) {
               const int c = 4 * c4 + e;
               const float z = ((keep >> c) & 1u) ? zs : 0.f;
-              ds[e] = pr[c] * (__uint_as_float(r[c]) * z - dv[e]);
+              ds[e] = pr[c] * (__uint_as_float(rdp[c]) * z - dv[e]);
             }
           } else {
-            sub2(ds[0], ds[1], __uint_as_float(r[4 * c4]), __uint_as_float(r[4 * c4 + 1]), dv[0], dv[1]);
-            sub2(ds[2], ds[3], __uint_as_float(r[4 * c4 + 2]), __uint_as_float(r[4 * c4 + 3]), dv[2], dv[3]);
+            sub2(ds[0], ds[1], __uint_as_float(rdp[4 * c4]), __uint_as_float(rdp[4 * c4 + 1]), dv[0], dv[1]);
+            sub2(ds[2], ds[3], __uint_as_float(rdp[4 * c4 + 2]), __uint_as_float(rdp[4 * c4 + 3]), dv[2], dv[3]);
             mul2(ds[0], ds[1], ds[0], ds[1], pr[4 * c4], pr[4 * c4 + 1]);
             mul2(ds[2], ds[3], ds[2], ds[3], pr[4 * c4 + 2], pr[4 * c4 + 3]);
           }
