@@ -18,14 +18,16 @@
 //   dK  += dS^T Q         same, A = dS^T in TMEM, B = Q
 //   dQ^T = K^T dS^T       M=128 d, N=64 queries, K=128 keys (A = K MN-major, B = dS^T)
 //
-// dQ^T is drained from TMEM and added into the fp32 dq_acc with coalesced
-// reductions (one 128-byte row segment per warp instruction); dK and dV stay
-// in TMEM for the whole item and are written once at the end.
+// dQ^T is drained from TMEM and added into the fp32 dq_acc with 16-byte
+// reductions (four 128-byte row segments per warp instruction); dK and dV
+// stay in TMEM for the whole item and are written once at the end.
 //
 // Warp roles (16 warps):
 //   0      TMA producer: K, V once; Q, dY, lse, D per query tile (3 stages)
-//   1      MMA issuer (one thread); the warp owns the TMEM allocation
-//   2-3    idle
+//   1      MMA issuer for S^T and dP^T (k-steps interleaved); owns the TMEM
+//          allocation
+//   2      MMA issuer for dV, then dK interleaved with dQ^T
+//   3      idle
 //   4-11   softmax: TMEM lane quarter = warp % 4 (one key per thread), column
 //          half = (warp - 4) / 4 (32 of the 64 queries); P, dropout, dS; then
 //          the dV (first half) / dK (second half) epilogue
@@ -562,13 +564,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // Thread (quad m, c) holds column d = quarter*32 + 4m + c for 64 queries.
       // A 4 x 4 transpose inside each quad (two xor-shuffle rounds) gives it
       // d = quarter*32 + 4m + 0..3 at query 4j + c, so that each reduction
-      // adds 16 contiguous bytes (4x fewer reduction instructions).
+      // adds 16 contiguous bytes (4x fewer reduction instructions).  All
+      // transposes come first, so that the 16 reductions issue back to back.
       const int rows = min(BM, sq.len_q - q0);
       const int c = lane & 3;
-      float *ptr = p.dq_acc + (int64_t(sq.cu_q) + q0 + c) * row_stride + int64_t(n) * HD +
-                   quarter * 32 + (lane & ~3);
+      float out[BM];
 #pragma unroll
-      for (int j = 0; j < BM / 4; ++j, ptr += 4 * row_stride) {
+      for (int j = 0; j < BM / 4; ++j) {
         const uint32_t *src = j < 8 ? a : b;
         const int o = 4 * (j & 7);
         const float x0 = __uint_as_float(src[o]), x1 = __uint_as_float(src[o + 1]);
@@ -580,9 +582,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const float r2 = hi2 ? x2 : t0, r3 = hi2 ? x3 : t1;
         const float u0 = __shfl_xor_sync(0xffffffffu, hi1 ? r0 : r1, 1);
         const float u1 = __shfl_xor_sync(0xffffffffu, hi1 ? r2 : r3, 1);
-        if (4 * j + c < rows)
-          red_add_v4_f32(ptr, hi1 ? u0 : r0, hi1 ? r1 : u0, hi1 ? u1 : r2, hi1 ? r3 : u1);
+        out[4 * j] = hi1 ? u0 : r0;
+        out[4 * j + 1] = hi1 ? r1 : u0;
+        out[4 * j + 2] = hi1 ? u1 : r2;
+        out[4 * j + 3] = hi1 ? r3 : u1;
       }
+      float *ptr = p.dq_acc + (int64_t(sq.cu_q) + q0 + c) * row_stride + int64_t(n) * HD +
+                   quarter * 32 + (lane & ~3);
+#pragma unroll
+      for (int j = 0; j < BM / 4; ++j, ptr += 4 * row_stride)
+        if (4 * j + c < rows)
+          red_add_v4_f32(ptr, out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
       if constexpr (kDet) {
         __threadfence();
         drain_bar_sync();
