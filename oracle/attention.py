@@ -47,6 +47,12 @@ Readings taken where the page is silent or ambiguous:
   ``D_i = sum_d dY_id * Y_id`` (Y = the attentionIn input).
 * Grouped heads (the constraint section allows Nq/Nkv integer): query head
   n reads key/value head ``n // (Nq / Nkv)``.
+* Outer split (the parameter table's qStartIdxOptional / kvStartIdxOptional:
+  the global start index of this chunk's query / key-value sequence).  The
+  window is evaluated on global positions: key j of the chunk is allowed
+  for query i iff ``(qs + i) - preTokens <= ks + j <= (qs + i) + nextTokens``
+  with qs, ks the chunk's starts (one pair per sequence, 0 when absent).
+  The keep-mask bits stay indexed by the chunk-local (i, j).
 """
 
 from __future__ import annotations
@@ -81,12 +87,13 @@ def mask_bit_offsets(lens_q, lens_kv, n_heads: int) -> np.ndarray:
 
 
 def window_allowed(lq: int, lk: int, pre_tokens: int, next_tokens: int,
-                   rows=None) -> np.ndarray:
+                   rows=None, q_start: int = 0, kv_start: int = 0) -> np.ndarray:
     """Allowed (i, j) pairs of one sequence for the preTokens/nextTokens
-    sliding window of the parameter table: ``i - pre <= j <= i + next``."""
+    sliding window of the parameter table, on global positions
+    ``gi = q_start + i``, ``gj = kv_start + j``: ``gi - pre <= gj <= gi + next``."""
     i = (np.arange(lq, dtype=np.int64) if rows is None
-         else np.asarray(rows, dtype=np.int64))[:, None]
-    j = np.arange(lk, dtype=np.int64)[None, :]
+         else np.asarray(rows, dtype=np.int64))[:, None] + int(q_start)
+    j = np.arange(lk, dtype=np.int64)[None, :] + int(kv_start)
     return (j >= i - pre_tokens) & (j <= i + next_tokens)
 
 
@@ -144,7 +151,7 @@ def _zscale(keep_rows, r0, r1, lk, keep_prob):
 
 
 def unit_forward(q, k, v, scale, pre_tokens, next_tokens, keep_rows=None,
-                 keep_prob=1.0, block=ROW_BLOCK):
+                 keep_prob=1.0, block=ROW_BLOCK, q_start=0, kv_start=0):
     """Y = Dropout(Softmax(S), keep_prob) V for one unit, plus the softmax
     statistics (max, sum) the forward hands to the backward.
 
@@ -157,7 +164,8 @@ def unit_forward(q, k, v, scale, pre_tokens, next_tokens, keep_rows=None,
     l = np.zeros(lq)
     for r0 in range(0, lq, block):
         r1 = min(lq, r0 + block)
-        allowed = window_allowed(lq, lk, pre_tokens, next_tokens, np.arange(r0, r1))
+        allowed = window_allowed(lq, lk, pre_tokens, next_tokens, np.arange(r0, r1),
+                                 q_start, kv_start)
         s = unit_logits(q[r0:r1], k, scale, allowed)
         mb, lb = _softmax_stats(s)
         p = _probs(s, mb, lb)
@@ -170,7 +178,7 @@ def unit_forward(q, k, v, scale, pre_tokens, next_tokens, keep_rows=None,
 
 def unit_backward(q, k, v, dy, y, m, l, scale, pre_tokens, next_tokens,
                   keep_rows=None, keep_prob=1.0, block=ROW_BLOCK,
-                  return_ds=False):
+                  return_ds=False, q_start=0, kv_start=0):
     """dQ, dK, dV of one unit from the backward formulas, using the given
     forward output ``y`` (attentionIn) and statistics ``m``/``l``.
 
@@ -189,7 +197,8 @@ def unit_backward(q, k, v, dy, y, m, l, scale, pre_tokens, next_tokens,
     dsum = (dy * y).sum(axis=1)
     for r0 in range(0, lq, block):
         r1 = min(lq, r0 + block)
-        allowed = window_allowed(lq, lk, pre_tokens, next_tokens, np.arange(r0, r1))
+        allowed = window_allowed(lq, lk, pre_tokens, next_tokens, np.arange(r0, r1),
+                                 q_start, kv_start)
         s = unit_logits(q[r0:r1], k, scale, allowed)
         p = _probs(s, m[r0:r1], l[r0:r1])
         z = _zscale(keep_rows, r0, r1, lk, keep_prob)
@@ -206,7 +215,7 @@ def unit_backward(q, k, v, dy, y, m, l, scale, pre_tokens, next_tokens,
 
 
 def unit_backward_rows(rows, q, k, v, dy, y, m, l, scale, pre_tokens,
-                       next_tokens, keep_rows=None, keep_prob=1.0):
+                       next_tokens, keep_rows=None, keep_prob=1.0, q_start=0, kv_start=0):
     """dQ at the given query rows only (each row of dS needs only its own
     row of S, dP and D)."""
     rows = np.asarray(rows, dtype=np.int64)
@@ -214,7 +223,7 @@ def unit_backward_rows(rows, q, k, v, dy, y, m, l, scale, pre_tokens,
     v = np.asarray(v, np.float64); dy = np.asarray(dy, np.float64)
     y = np.asarray(y, np.float64)
     lq, lk = q.shape[0], k.shape[0]
-    allowed = window_allowed(lq, lk, pre_tokens, next_tokens, rows)
+    allowed = window_allowed(lq, lk, pre_tokens, next_tokens, rows, q_start, kv_start)
     s = unit_logits(q[rows], k, scale, allowed)
     p = _probs(s, np.asarray(m, np.float64)[rows], np.asarray(l, np.float64)[rows])
     if keep_rows is None or keep_prob >= 1.0:
@@ -228,7 +237,7 @@ def unit_backward_rows(rows, q, k, v, dy, y, m, l, scale, pre_tokens,
 
 
 def unit_backward_cols(cols, q, k, v, dy, y, m, l, scale, pre_tokens,
-                       next_tokens, keep_cols=None, keep_prob=1.0):
+                       next_tokens, keep_cols=None, keep_prob=1.0, q_start=0, kv_start=0):
     """dK and dV at the given key rows only (column j of P and dS runs over
     every query row i, so the full statistics m, l and D are used).
 
@@ -239,8 +248,8 @@ def unit_backward_cols(cols, q, k, v, dy, y, m, l, scale, pre_tokens,
     y = np.asarray(y, np.float64)
     m = np.asarray(m, np.float64); l = np.asarray(l, np.float64)
     lq, lk = q.shape[0], k.shape[0]
-    i = np.arange(lq, dtype=np.int64)[:, None]
-    j = cols[None, :]
+    i = np.arange(lq, dtype=np.int64)[:, None] + int(q_start)
+    j = cols[None, :] + int(kv_start)
     allowed = (j >= i - pre_tokens) & (j <= i + next_tokens)
     s = np.where(allowed, scale * (q @ k[cols].T), -np.inf)
     p = _probs(s, m, l)
@@ -268,10 +277,17 @@ def _keep_fns(mask_u8, bit_off, lq, lk):
     return rows_fn, cols_fn
 
 
+def _starts(starts, batch):
+    return [0] * batch if starts is None else [int(x) for x in starts]
+
+
 def varlen_forward(q, k, v, lens_q, lens_kv, scale, pre_tokens, next_tokens,
-                   mask_u8=None, keep_prob=1.0):
+                   mask_u8=None, keep_prob=1.0, q_start=None, kv_start=None):
     """Forward over a packed batch: q [Tq, N, D], k/v [Tk, Nkv, D*].
+    ``q_start`` / ``kv_start``: per-sequence global start indices of the
+    chunks (outer split), or None for zeros.
     Returns y [Tq, N, Dv], softmax_max [Tq, N, 8], softmax_sum [Tq, N, 8]."""
+    qs0, ks0 = _starts(q_start, len(lens_q)), _starts(kv_start, len(lens_q))
     q = np.asarray(q, np.float64); k = np.asarray(k, np.float64)
     v = np.asarray(v, np.float64)
     n_heads, n_kv = q.shape[1], k.shape[1]
@@ -290,7 +306,8 @@ def varlen_forward(q, k, v, lens_q, lens_kv, scale, pre_tokens, next_tokens,
             rows_fn, _ = _keep_fns(mask_u8, int(offs[b]) + n * lq * lk, lq, lk)
             yb, mb, lb = unit_forward(q[cq[b]:cq[b + 1], n], k[ck[b]:ck[b + 1], kv],
                                       v[ck[b]:ck[b + 1], kv], scale, pre_tokens,
-                                      next_tokens, rows_fn, keep_prob)
+                                      next_tokens, rows_fn, keep_prob,
+                                      q_start=qs0[b], kv_start=ks0[b])
             y[cq[b]:cq[b + 1], n] = yb
             smax[cq[b]:cq[b + 1], n, :] = mb[:, None]
             ssum[cq[b]:cq[b + 1], n, :] = lb[:, None]
@@ -298,10 +315,12 @@ def varlen_forward(q, k, v, lens_q, lens_kv, scale, pre_tokens, next_tokens,
 
 
 def varlen_backward(q, k, v, dy, y, softmax_max, softmax_sum, lens_q, lens_kv,
-                    scale, pre_tokens, next_tokens, mask_u8=None, keep_prob=1.0):
+                    scale, pre_tokens, next_tokens, mask_u8=None, keep_prob=1.0,
+                    q_start=None, kv_start=None):
     """Backward over a packed batch; reads lane 0 of the [T, N, 8] statistics.
     Returns dq [Tq, N, D], dk [Tk, Nkv, D], dv [Tk, Nkv, Dv] (grouped query
     heads add into their shared key/value head)."""
+    qs0, ks0 = _starts(q_start, len(lens_q)), _starts(kv_start, len(lens_q))
     q = np.asarray(q, np.float64); k = np.asarray(k, np.float64)
     v = np.asarray(v, np.float64); dy = np.asarray(dy, np.float64)
     y = np.asarray(y, np.float64)
@@ -325,7 +344,7 @@ def varlen_backward(q, k, v, dy, y, softmax_max, softmax_sum, lens_q, lens_kv,
             dqb, dkb, dvb = unit_backward(q[qs, n], k[ks, kv], v[ks, kv], dy[qs, n],
                                           y[qs, n], smax[qs, n, 0], ssum[qs, n, 0],
                                           scale, pre_tokens, next_tokens, rows_fn,
-                                          keep_prob)
+                                          keep_prob, q_start=qs0[b], kv_start=ks0[b])
             dq[qs, n] = dqb
             dk[ks, kv] += dkb
             dv[ks, kv] += dvb

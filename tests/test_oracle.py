@@ -357,3 +357,76 @@ def test_workload_shapes():
     assert wl.workload(5).mask_bits == 4 * 16 * 16384 * 16384
     q, k, v, dy = wl.make_tensors(wl.workload(1))
     assert q.shape == (101, 2, 64) and q.dtype == torch.float32
+
+
+# ---------------------------------------------------------------------------
+# outer split (qStartIdx / kvStartIdx)
+# ---------------------------------------------------------------------------
+
+def test_window_split_fixture():
+    for c in _load("window_split_cases.json")["cases"]:
+        got = oracle.window_allowed(c["lq"], c["lk"], c["pre"], c["next"],
+                                    q_start=c["q_start"], kv_start=c["kv_start"])
+        assert got.astype(int).tolist() == c["allowed"], c
+
+
+@pytest.mark.parametrize("pre,nxt", [(2 ** 31 - 1, 0), (20, 5)])
+def test_query_chunks_reproduce_the_whole_sequence(pre, nxt):
+    """Cutting one sequence's queries into chunks, each run against the whole
+    key/value sequence with its global start, reproduces the rows of the
+    whole run (forward and dQ), and the chunks' dK, dV add up to the whole
+    run's: the context-parallel use the outer-split parameters exist for."""
+    rng = np.random.default_rng(11)
+    L, n, d, cut = 70, 2, 8, 33
+    q, k, v, dy = (rng.standard_normal((L, n, d)) for _ in range(4))
+    sc = 0.3
+    y, m, l = oracle.varlen_forward(q, k, v, [L], [L], sc, pre, nxt)
+    dq, dk, dv = oracle.varlen_backward(q, k, v, dy, y, m, l, [L], [L], sc, pre, nxt)
+    dk_sum, dv_sum = np.zeros_like(dk), np.zeros_like(dv)
+    for a, b in ((0, cut), (cut, L)):
+        yc, mc, lc = oracle.varlen_forward(q[a:b], k, v, [b - a], [L], sc, pre, nxt,
+                                           q_start=[a], kv_start=[0])
+        np.testing.assert_allclose(yc, y[a:b], rtol=0, atol=1e-12)
+        np.testing.assert_array_equal(np.isinf(mc), np.isinf(m[a:b]))
+        np.testing.assert_allclose(lc, l[a:b], rtol=1e-12, atol=0)
+        dqc, dkc, dvc = oracle.varlen_backward(q[a:b], k, v, dy[a:b], yc, mc, lc, [b - a], [L],
+                                               sc, pre, nxt, q_start=[a], kv_start=[0])
+        np.testing.assert_allclose(dqc, dq[a:b], rtol=0, atol=1e-12)
+        dk_sum += dkc
+        dv_sum += dvc
+    np.testing.assert_allclose(dk_sum, dk, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv_sum, dv, rtol=0, atol=1e-12)
+
+
+def test_key_chunks_reproduce_the_whole_sequence():
+    """With the whole run's statistics, backward over key/value chunks (each
+    with its global start) gives the whole run's dK, dV rows, and the
+    chunks' dQ add up to the whole run's dQ."""
+    rng = np.random.default_rng(12)
+    L, n, d, cut = 64, 2, 8, 29
+    q, k, v, dy = (rng.standard_normal((L, n, d)) for _ in range(4))
+    sc, pre, nxt = 0.25, 2 ** 31 - 1, 0
+    y, m, l = oracle.varlen_forward(q, k, v, [L], [L], sc, pre, nxt)
+    dq, dk, dv = oracle.varlen_backward(q, k, v, dy, y, m, l, [L], [L], sc, pre, nxt)
+    dq_sum = np.zeros_like(dq)
+    for a, b in ((0, cut), (cut, L)):
+        dqc, dkc, dvc = oracle.varlen_backward(q, k[a:b], v[a:b], dy, y, m, l, [L], [b - a],
+                                               sc, pre, nxt, q_start=[0], kv_start=[a])
+        np.testing.assert_allclose(dkc, dk[a:b], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dvc, dv[a:b], rtol=0, atol=1e-12)
+        dq_sum += dqc
+    np.testing.assert_allclose(dq_sum, dq, rtol=0, atol=1e-12)
+
+
+def test_equal_starts_change_nothing():
+    """Only the difference of the two starts matters: shifting both by the
+    same amount leaves every output unchanged."""
+    rng = np.random.default_rng(13)
+    lens = [23, 17]
+    T = sum(lens)
+    q, k, v, dy = (rng.standard_normal((T, 2, 8)) for _ in range(4))
+    base = oracle.varlen_forward(q, k, v, lens, lens, 0.3, 5, 2)
+    moved = oracle.varlen_forward(q, k, v, lens, lens, 0.3, 5, 2, q_start=[100, 7],
+                                  kv_start=[100, 7])
+    for a, b in zip(base, moved):
+        np.testing.assert_array_equal(a, b)
