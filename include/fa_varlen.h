@@ -112,7 +112,22 @@ typedef struct {
    * `stream` before the preprocess kernel, before the main kernel, after the
    * main kernel and after the dQ convert kernel, for per-kernel timing. */
   void *const *events;
+  /* Outer split (the parameter table's qStartIdxOptional / kvStartIdxOptional):
+   * host arrays of `batch` global start indices (>= 0) of each sequence's
+   * query / key-value chunk, or NULL for 0.  The window is then evaluated on
+   * global positions: key j of the chunk is allowed for query i iff
+   * (qs + i) - pre_tokens <= ks + j <= (qs + i) + next_tokens.  Dropout bits
+   * stay indexed by the chunk-local (i, j).  A negative start is
+   * FA_ERR_INVALID.  The forward must be given the same starts. */
+  const int64_t *q_start_idx;
+  const int64_t *kv_start_idx;
 } fa_bwd_options;
+
+/* Options of fa_varlen_fwd_ex. */
+typedef struct {
+  const int64_t *q_start_idx;   /* as in fa_bwd_options; NULL for 0 */
+  const int64_t *kv_start_idx;
+} fa_fwd_options;
 
 /* Forward workspace size in bytes (same scalar arguments as fa_varlen_fwd). */
 fa_status fa_varlen_fwd_workspace_size(
@@ -133,6 +148,19 @@ fa_status fa_varlen_fwd(
     int64_t sparse_mode,
     void *y, float *softmax_max, float *softmax_sum,
     void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/* fa_varlen_fwd with options (NULL = defaults); same workspace size. */
+fa_status fa_varlen_fwd_ex(
+    const void *q, const void *k, const void *v,
+    const uint8_t *drop_mask, int64_t drop_mask_bytes,
+    const int64_t *seq_lens_q, const int64_t *seq_lens_kv, int64_t batch,
+    int64_t total_q, int64_t total_kv, int64_t head_num, int64_t head_num_kv,
+    int64_t head_dim, fa_dtype dtype, const char *layout, double scale,
+    double keep_prob, int64_t pre_tokens, int64_t next_tokens,
+    int64_t sparse_mode,
+    void *y, float *softmax_max, float *softmax_sum,
+    void *workspace, size_t workspace_bytes, fa_stream_t stream,
+    const fa_fwd_options *options);
 
 /* Backward workspace size in bytes.  Depends on the lengths, head counts,
  * head_dim and the kernel AUTO would choose for `dtype`. */

@@ -36,12 +36,14 @@ def device_mask(w: wl.Workload, dev):
     return fa.gen_keep_mask(w.mask_bits, w.mask_seed, w.keep_prob, device=dev)
 
 
-def gpu_forward_backward(w: wl.Workload, tensors, dev, impl=fa.FA_BWD_AUTO, mask=None):
+def gpu_forward_backward(w: wl.Workload, tensors, dev, impl=fa.FA_BWD_AUTO, mask=None,
+                         q_start=None, kv_start=None):
     q, k, v, dy = (t.to(dev) for t in tensors)
     y, smax, ssum = fa.fwd(q, k, v, w.lens, w.lens_kv, w.scale, w.pre_tokens, w.next_tokens,
-                           w.keep_prob, mask)
+                           w.keep_prob, mask, q_start=q_start, kv_start=kv_start)
     dq, dk, dv = fa.bwd(q, k, v, dy, y, smax, ssum, w.lens, w.lens_kv, w.scale, w.pre_tokens,
-                        w.next_tokens, w.keep_prob, mask, impl=impl)
+                        w.next_tokens, w.keep_prob, mask, impl=impl, q_start=q_start,
+                        kv_start=kv_start)
     torch.cuda.synchronize()
     return dict(y=y, smax=smax, ssum=ssum, dq=dq, dk=dk, dv=dv)
 
@@ -67,13 +69,15 @@ def cpu_keep_rows(w: wl.Workload, b: int, n: int):
     return rows, cols
 
 
-def oracle_full(w: wl.Workload, tensors, mask_np=None):
+def oracle_full(w: wl.Workload, tensors, mask_np=None, q_start=None, kv_start=None):
     """Oracle forward + backward over the whole packed batch."""
     q, k, v, dy = (f64(t) for t in tensors)
     y, m, l = oracle.varlen_forward(q, k, v, w.lens, w.lens_kv, w.scale, w.pre_tokens,
-                                    w.next_tokens, mask_np, w.keep_prob)
+                                    w.next_tokens, mask_np, w.keep_prob, q_start=q_start,
+                                    kv_start=kv_start)
     dq, dk, dv = oracle.varlen_backward(q, k, v, dy, y, m, l, w.lens, w.lens_kv, w.scale,
-                                        w.pre_tokens, w.next_tokens, mask_np, w.keep_prob)
+                                        w.pre_tokens, w.next_tokens, mask_np, w.keep_prob,
+                                        q_start=q_start, kv_start=kv_start)
     return dict(y=y, smax=m, ssum=l, dq=dq, dk=dk, dv=dv)
 
 

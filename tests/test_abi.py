@@ -237,3 +237,21 @@ def test_deterministic_option_accepted():
                                                     BIG, 0, ctypes.byref(opt),
                                                     ctypes.byref(out)) == fa.FA_OK
     assert out.value > 0
+
+
+def test_negative_chunk_start_is_invalid():
+    lq = (ctypes.c_int64 * 1)(8)
+    out = ctypes.c_size_t(0)
+    neg = (ctypes.c_int64 * 1)(-1)
+    opt = fa.BwdOptions(fa.FA_BWD_AUTO, 0, 0, None,
+                        ctypes.cast(neg, ctypes.POINTER(ctypes.c_int64)), None)
+    assert fa.lib().fa_varlen_bwd_workspace_size_ex(lq, lq, 1, 8, 8, 1, 1, 64,
+                                                    fa._DTYPE[torch.float32], b"TND", 1.0, BIG,
+                                                    BIG, 0, ctypes.byref(opt),
+                                                    ctypes.byref(out)) == fa.FA_ERR_INVALID
+    fake = ctypes.c_void_p(0x1000)
+    fo = fa.FwdOptions(ctypes.cast(neg, ctypes.POINTER(ctypes.c_int64)), None)
+    st = fa.lib().fa_varlen_fwd_ex(fake, fake, fake, None, 0, lq, lq, 1, 8, 8, 1, 1, 64,
+                                   fa._DTYPE[torch.float32], b"TND", 0.125, 1.0, BIG, BIG, 0,
+                                   fake, fake, fake, fake, 1 << 20, None, ctypes.byref(fo))
+    assert st == fa.FA_ERR_INVALID

@@ -31,7 +31,14 @@ _psz = ctypes.POINTER(ctypes.c_size_t)
 
 class BwdOptions(ctypes.Structure):
     _fields_ = [("impl", ctypes.c_int32), ("deterministic", ctypes.c_int32),
-                ("wait_timeout_ns", ctypes.c_int64), ("events", ctypes.POINTER(ctypes.c_void_p))]
+                ("wait_timeout_ns", ctypes.c_int64), ("events", ctypes.POINTER(ctypes.c_void_p)),
+                ("q_start_idx", ctypes.POINTER(ctypes.c_int64)),
+                ("kv_start_idx", ctypes.POINTER(ctypes.c_int64))]
+
+
+class FwdOptions(ctypes.Structure):
+    _fields_ = [("q_start_idx", ctypes.POINTER(ctypes.c_int64)),
+                ("kv_start_idx", ctypes.POINTER(ctypes.c_int64))]
 
 
 class FaError(RuntimeError):
@@ -51,6 +58,9 @@ _SIGS = {
         _SCALARS + [_f64, _i64, _i64, _i64, ctypes.POINTER(BwdOptions), _psz], _i32),
     "fa_varlen_fwd": ([_vp, _vp, _vp, _vp, _i64] + _SCALARS[:8] + [_i32, _cp, _f64, _f64, _i64,
                       _i64, _i64, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "fa_varlen_fwd_ex": ([_vp, _vp, _vp, _vp, _i64] + _SCALARS[:8] + [_i32, _cp, _f64, _f64,
+                         _i64, _i64, _i64, _vp, _vp, _vp, _vp, _sz, _vp,
+                         ctypes.POINTER(FwdOptions)], _i32),
     "fa_varlen_bwd": ([_vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp] + _SCALARS[:8] +
                       [_i32, _cp, _f64, _f64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _sz, _vp],
                       _i32),
@@ -119,13 +129,27 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _opts(impl=FA_BWD_AUTO, wait_timeout_ns=0, events=None, deterministic=False):
+def _starts(starts):
+    """Host int64 array of per-sequence chunk starts, or None."""
+    if starts is None:
+        return None
+    vals = [int(x) for x in starts]
+    return (ctypes.c_int64 * max(1, len(vals)))(*vals)
+
+
+def _opts(impl=FA_BWD_AUTO, wait_timeout_ns=0, events=None, deterministic=False,
+          q_start=None, kv_start=None):
     ev = None
     if events is not None:
         arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
         ev = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
         ev._keep = arr
-    return BwdOptions(int(impl), int(bool(deterministic)), int(wait_timeout_ns), ev)
+    qs, ks = _starts(q_start), _starts(kv_start)
+    opt = BwdOptions(int(impl), int(bool(deterministic)), int(wait_timeout_ns), ev,
+                     ctypes.cast(qs, ctypes.POINTER(ctypes.c_int64)) if qs is not None else None,
+                     ctypes.cast(ks, ctypes.POINTER(ctypes.c_int64)) if ks is not None else None)
+    opt._keep = (qs, ks)
+    return opt
 
 
 def fwd_workspace_size(lens_q, lens_kv, n, n_kv, d, dtype, keep_prob=1.0,
@@ -155,8 +179,9 @@ def bwd_workspace_size(lens_q, lens_kv, n, n_kv, d, dtype, keep_prob=1.0,
 
 def fwd(q, k, v, lens_q, lens_kv, scale, pre_tokens, next_tokens, keep_prob=1.0,
         drop_mask=None, y=None, softmax_max=None, softmax_sum=None, workspace=None,
-        stream=None):
-    """Y and the [T, N, 8] statistics (fa_varlen_fwd)."""
+        stream=None, q_start=None, kv_start=None):
+    """Y and the [T, N, 8] statistics (fa_varlen_fwd_ex).  ``q_start`` /
+    ``kv_start``: per-sequence global chunk starts (outer split), or None."""
     tq, n, d = q.shape
     n_kv = k.shape[1]
     lq, b, _ = _lens(lens_q)
@@ -173,18 +198,22 @@ def fwd(q, k, v, lens_q, lens_kv, scale, pre_tokens, next_tokens, keep_prob=1.0,
                                 next_tokens)
         workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
     mask_bytes = 0 if drop_mask is None else drop_mask.numel()
-    _check(lib().fa_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(drop_mask), mask_bytes, lq, lk, b,
-                               tq, k.shape[0], n, n_kv, d, _DTYPE[q.dtype], b"TND", float(scale),
-                               float(keep_prob), int(pre_tokens), int(next_tokens), 0, _ptr(y),
-                               _ptr(softmax_max), _ptr(softmax_sum), _ptr(workspace),
-                               workspace.numel(), _stream(stream)), "fa_varlen_fwd")
+    qs, ks = _starts(q_start), _starts(kv_start)
+    opt = FwdOptions(ctypes.cast(qs, ctypes.POINTER(ctypes.c_int64)) if qs is not None else None,
+                     ctypes.cast(ks, ctypes.POINTER(ctypes.c_int64)) if ks is not None else None)
+    _check(lib().fa_varlen_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(drop_mask), mask_bytes, lq, lk,
+                                  b, tq, k.shape[0], n, n_kv, d, _DTYPE[q.dtype], b"TND",
+                                  float(scale), float(keep_prob), int(pre_tokens),
+                                  int(next_tokens), 0, _ptr(y), _ptr(softmax_max),
+                                  _ptr(softmax_sum), _ptr(workspace), workspace.numel(),
+                                  _stream(stream), ctypes.byref(opt)), "fa_varlen_fwd_ex")
     return y, softmax_max, softmax_sum
 
 
 def bwd(q, k, v, dy, y, softmax_max, softmax_sum, lens_q, lens_kv, scale, pre_tokens,
         next_tokens, keep_prob=1.0, drop_mask=None, dq=None, dk=None, dv=None,
         workspace=None, stream=None, impl=FA_BWD_AUTO, wait_timeout_ns=0, events=None,
-        deterministic=False):
+        deterministic=False, q_start=None, kv_start=None):
     """dQ, dK, dV (fa_varlen_bwd_ex).  ``events``: four torch.cuda.Event
     (already recorded once, so that they exist) recorded around the kernels.
     ``deterministic``: add the dQ partials in a fixed order (bitwise
@@ -204,7 +233,7 @@ def bwd(q, k, v, dy, y, softmax_max, softmax_sum, lens_q, lens_kv, scale, pre_to
                                 next_tokens, impl)
         workspace = torch.empty(ws, dtype=torch.uint8, device=q.device)
     mask_bytes = 0 if drop_mask is None else drop_mask.numel()
-    opt = _opts(impl, wait_timeout_ns, events, deterministic)
+    opt = _opts(impl, wait_timeout_ns, events, deterministic, q_start, kv_start)
     _check(lib().fa_varlen_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(dy), _ptr(drop_mask),
                                   mask_bytes, _ptr(softmax_max), _ptr(softmax_sum), _ptr(y), lq,
                                   lk, b, tq, k.shape[0], n, n_kv, d, _DTYPE[q.dtype], b"TND",

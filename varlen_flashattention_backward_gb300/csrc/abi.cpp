@@ -25,9 +25,11 @@ constexpr long long kDefaultTimeoutNs = 2000000000LL;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
-int clamp_window(int64_t x) {
-  const int64_t lim = int64_t(1) << 30;
-  return int(std::max(-lim, std::min(lim, x)));
+// Window bounds beyond +-2^28 act like unbounded ones (lengths are below
+// 2^20), and keep index arithmetic inside int32 on the device.
+int64_t clamp_window(int64_t x) {
+  const int64_t lim = int64_t(1) << 28;
+  return std::max(-lim, std::min(lim, x));
 }
 
 struct Problem {
@@ -38,6 +40,16 @@ struct Problem {
   int64_t pre, next, sparse_mode;
   int64_t tp;         // padded statistics rows
   int64_t mask_bits;
+  // Outer split: per-sequence global start of the query / key-value chunk
+  // (host arrays of length batch), or null for 0.
+  const int64_t *q_start = nullptr, *kv_start = nullptr;
+
+  // Window of sequence b on chunk-local indices (see SeqInfo::pre).
+  int64_t shift(int64_t b) const {
+    return (q_start ? q_start[b] : 0) - (kv_start ? kv_start[b] : 0);
+  }
+  int64_t pre_of(int64_t b) const { return clamp_window(clamp_window(pre) - shift(b)); }
+  int64_t next_of(int64_t b) const { return clamp_window(clamp_window(next) + shift(b)); }
 };
 
 // Checks shared by every entry point.  `need_ptrs` lists pointers that must
@@ -67,6 +79,9 @@ fa_status check_problem(Problem &pr, const char *layout,
     bits += pr.n * lq * lk;
   }
   if (sq != pr.total_q || sk != pr.total_kv) return FA_ERR_INVALID;
+  for (int64_t b = 0; b < pr.batch; ++b)
+    if ((pr.q_start && pr.q_start[b] < 0) || (pr.kv_start && pr.kv_start[b] < 0))
+      return FA_ERR_INVALID;
   if (pr.sparse_mode != 0) return FA_ERR_UNSUPPORTED;
   if (pr.d != 64 && pr.d != 128) return FA_ERR_UNSUPPORTED;
   pr.tp = tp;
@@ -84,6 +99,8 @@ std::vector<SeqInfo> build_seqs(const Problem &pr) {
     s[b].len_q = int32_t(lq);
     s[b].len_k = int32_t(lk);
     s[b].qpad = int32_t(qp);
+    s[b].pre = int32_t(pr.pre_of(b));
+    s[b].next = int32_t(pr.next_of(b));
     s[b].pad_ = 0;
     s[b].mask_off = mo;
     cq += lq;
@@ -124,8 +141,8 @@ std::vector<WorkItem> build_bwd_items(const Problem &pr, int kv_tile, bool tile_
       Unit u{items.size(), size_t(tiles), 0};
       for (int64_t t = 0; t < tiles; ++t) {
         const int64_t k0 = t * kv_tile, k1 = std::min(lk, k0 + kv_tile);
-        const int64_t lo = std::max<int64_t>(0, k0 - pr.next);
-        const int64_t hi = std::min<int64_t>(lq - 1, k1 - 1 + pr.pre);
+        const int64_t lo = std::max<int64_t>(0, k0 - pr.next_of(b));
+        const int64_t hi = std::min<int64_t>(lq - 1, k1 - 1 + pr.pre_of(b));
         int64_t qlo = 0, cnt = 0;
         if (lq > 0 && lo <= hi) {
           qlo = lo / kQTile;
@@ -160,8 +177,8 @@ std::vector<WorkItem> build_fwd_items(const Problem &pr) {
     const int64_t tiles = ceil_div(lq, kQTile);
     for (int64_t t = 0; t < tiles; ++t) {
       const int64_t q0 = t * kQTile, q1 = std::min(lq, q0 + kQTile);
-      const int64_t lo = std::max<int64_t>(0, q0 - pr.pre);
-      const int64_t hi = std::min<int64_t>(lk - 1, q1 - 1 + pr.next);
+      const int64_t lo = std::max<int64_t>(0, q0 - pr.pre_of(b));
+      const int64_t hi = std::min<int64_t>(lk - 1, q1 - 1 + pr.next_of(b));
       int64_t klo = 0, cnt = 0;
       if (lk > 0 && lo <= hi) {
         klo = lo / kSimtKvTile;
@@ -318,16 +335,22 @@ fa_status fa_varlen_fwd_workspace_size(const int64_t *seq_lens_q, const int64_t 
   return FA_OK;
 }
 
-fa_status fa_varlen_fwd(const void *q, const void *k, const void *v, const uint8_t *drop_mask,
-                        int64_t drop_mask_bytes, const int64_t *seq_lens_q,
-                        const int64_t *seq_lens_kv, int64_t batch, int64_t total_q,
-                        int64_t total_kv, int64_t head_num, int64_t head_num_kv,
-                        int64_t head_dim, fa_dtype dtype, const char *layout, double scale,
-                        double keep_prob, int64_t pre_tokens, int64_t next_tokens,
-                        int64_t sparse_mode, void *y, float *softmax_max, float *softmax_sum,
-                        void *workspace, size_t workspace_bytes, fa_stream_t stream) {
+fa_status fa_varlen_fwd_ex(const void *q, const void *k, const void *v,
+                           const uint8_t *drop_mask, int64_t drop_mask_bytes,
+                           const int64_t *seq_lens_q, const int64_t *seq_lens_kv,
+                           int64_t batch, int64_t total_q, int64_t total_kv, int64_t head_num,
+                           int64_t head_num_kv, int64_t head_dim, fa_dtype dtype,
+                           const char *layout, double scale, double keep_prob,
+                           int64_t pre_tokens, int64_t next_tokens, int64_t sparse_mode,
+                           void *y, float *softmax_max, float *softmax_sum, void *workspace,
+                           size_t workspace_bytes, fa_stream_t stream,
+                           const fa_fwd_options *options) {
   Problem pr{seq_lens_q, seq_lens_kv, batch, total_q, total_kv, head_num, head_num_kv,
              head_dim, dtype, keep_prob, pre_tokens, next_tokens, sparse_mode, 0, 0};
+  if (options) {
+    pr.q_start = options->q_start_idx;
+    pr.kv_start = options->kv_start_idx;
+  }
   // Pointers of an empty side (no query rows / no key rows) may be null.
   const bool hq = total_q > 0, hk = total_kv > 0;
   const void *ok = &pr;
@@ -360,12 +383,25 @@ fa_status fa_varlen_fwd(const void *q, const void *k, const void *v, const uint8
   p.items = reinterpret_cast<const WorkItem *>(ws + items_off);
   p.n_items = int(items.size());
   p.batch = int(batch); p.n = int(head_num); p.n_kv = int(head_num_kv); p.d = int(head_dim);
-  p.pre = clamp_window(pre_tokens); p.next = clamp_window(next_tokens);
   p.scale = float(scale);
   p.inv_keep = float(1.0 / keep_prob);
   p.use_dropout = dropout;
   if (launch_fwd_simt(p, dtype, cs) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
+}
+
+fa_status fa_varlen_fwd(const void *q, const void *k, const void *v, const uint8_t *drop_mask,
+                        int64_t drop_mask_bytes, const int64_t *seq_lens_q,
+                        const int64_t *seq_lens_kv, int64_t batch, int64_t total_q,
+                        int64_t total_kv, int64_t head_num, int64_t head_num_kv,
+                        int64_t head_dim, fa_dtype dtype, const char *layout, double scale,
+                        double keep_prob, int64_t pre_tokens, int64_t next_tokens,
+                        int64_t sparse_mode, void *y, float *softmax_max, float *softmax_sum,
+                        void *workspace, size_t workspace_bytes, fa_stream_t stream) {
+  return fa_varlen_fwd_ex(q, k, v, drop_mask, drop_mask_bytes, seq_lens_q, seq_lens_kv, batch,
+                          total_q, total_kv, head_num, head_num_kv, head_dim, dtype, layout,
+                          scale, keep_prob, pre_tokens, next_tokens, sparse_mode, y,
+                          softmax_max, softmax_sum, workspace, workspace_bytes, stream, nullptr);
 }
 
 fa_status fa_varlen_bwd_workspace_size_ex(const int64_t *seq_lens_q, const int64_t *seq_lens_kv,
@@ -379,6 +415,10 @@ fa_status fa_varlen_bwd_workspace_size_ex(const int64_t *seq_lens_q, const int64
   if (workspace_bytes == nullptr) return FA_ERR_NULLPTR;
   Problem pr{seq_lens_q, seq_lens_kv, batch, total_q, total_kv, head_num, head_num_kv,
              head_dim, dtype, keep_prob, pre_tokens, next_tokens, sparse_mode, 0, 0};
+  if (options) {
+    pr.q_start = options->q_start_idx;
+    pr.kv_start = options->kv_start_idx;
+  }
   fa_status st = check_problem(pr, layout, {});
   if (st != FA_OK) return st;
   if (options && (options->impl < FA_BWD_AUTO || options->impl > FA_BWD_TCGEN05))
@@ -415,6 +455,10 @@ fa_status fa_varlen_bwd_ex(const void *q, const void *k, const void *v, const vo
                            const fa_bwd_options *options) {
   Problem pr{seq_lens_q, seq_lens_kv, batch, total_q, total_kv, head_num, head_num_kv,
              head_dim, dtype, keep_prob, pre_tokens, next_tokens, sparse_mode, 0, 0};
+  if (options) {
+    pr.q_start = options->q_start_idx;
+    pr.kv_start = options->kv_start_idx;
+  }
   // Pointers of an empty side (no query rows / no key rows) may be null.
   const bool hq = total_q > 0, hk = total_kv > 0;
   const void *ok = &pr;
@@ -475,7 +519,6 @@ fa_status fa_varlen_bwd_ex(const void *q, const void *k, const void *v, const vo
   p.n_items = int(items.size());
   p.batch = int(batch); p.n = int(head_num); p.n_kv = int(head_num_kv); p.d = int(head_dim);
   p.tp = int(pr.tp); p.total_q = int(total_q); p.total_kv = int(total_kv);
-  p.pre = clamp_window(pre_tokens); p.next = clamp_window(next_tokens);
   p.scale = float(scale);
   p.scale_log2 = float(scale * 1.4426950408889634);
   p.inv_keep = float(1.0 / keep_prob);

@@ -411,13 +411,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           pr[4 * c4 + 3] = ex2(pr[4 * c4 + 3]);
         }
       }
-      const bool full_tile = (k0 + BN - 1 <= q0 + p.next) && (k0 >= q0 + BM - 1 - p.pre) &&
+      const bool full_tile = (k0 + BN - 1 <= q0 + sq.next) && (k0 >= q0 + BM - 1 - sq.pre) &&
                              (k0 + BN <= sq.len_k);
       if (!full_tile) {
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           const int i = i0 + c;
-          if (!(jg <= i + p.next && jg >= i - p.pre && jg < sq.len_k)) pr[c] = 0.f;
+          if (!(jg <= i + sq.next && jg >= i - sq.pre && jg < sq.len_k)) pr[c] = 0.f;
         }
       }
       uint32_t keep = 0xFFFFFFFFu;

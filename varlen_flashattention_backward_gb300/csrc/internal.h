@@ -13,16 +13,23 @@ constexpr int kSimtKvTile = 64;   // key rows per work item, CUDA-core kernels
 constexpr int kTcKvTile = 128;    // key rows per work item, tcgen05 kernel
 constexpr int kMaxBatch = 2048;
 
-// One per sequence, uploaded into the workspace (32 bytes).
+// One per sequence, uploaded into the workspace (40 bytes).
 struct SeqInfo {
   int32_t cu_q;      // first row of the sequence in q / dy / y / dq
   int32_t cu_k;      // first row in k / v / dk / dv
   int32_t len_q;
   int32_t len_k;
   int32_t qpad;      // first row in the 64-row-padded statistics index space
-  int32_t pad_;
+  // Window of this sequence on chunk-local indices: key j is allowed for
+  // query i iff i - pre <= j <= i + next.  preTokens / nextTokens shifted by
+  // the chunk starts (pre - (qs - ks), next + (qs - ks)), clamped to +-2^28,
+  // which keeps every sum with an index inside int32.
+  int32_t pre;
   int64_t mask_off;  // dropout bit of (head 0, i 0, j 0): N * sum_{b'<b} Lq*Lk
+  int32_t next;
+  int32_t pad_;
 };
+static_assert(sizeof(SeqInfo) == 40, "SeqInfo layout");
 
 // One unit of work.  Backward: key tile `tile` of sequence `seq` for key/value
 // head `head`, covering query tiles [lo, lo + count) of every query head of
@@ -70,7 +77,6 @@ struct BwdParams {
   int32_t *sem;
   const int32_t *qfirst;
   int n_items, batch, n, n_kv, d, tp, total_q, total_kv;
-  int pre, next;    // clamped to +-2^30
   float scale, scale_log2, inv_keep;
   int use_dropout;
   long long timeout_ns;
@@ -85,7 +91,6 @@ struct FwdParams {
   const SeqInfo *seqs;
   const WorkItem *items;
   int n_items, batch, n, n_kv, d;
-  int pre, next;
   float scale, inv_keep;
   int use_dropout;
 };
