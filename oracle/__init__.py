@@ -19,6 +19,7 @@ unpinned".
 """
 
 from .attention import (  # noqa: F401
+    mode_window,
     window_allowed,
     keep_bits_unit,
     unit_logits,

@@ -47,6 +47,14 @@ Readings taken where the page is silent or ambiguous:
   ``D_i = sum_d dY_id * Y_id`` (Y = the attentionIn input).
 * Grouped heads (the constraint section allows Nq/Nkv integer): query head
   n reads key/value head ``n // (Nq / Nkv)``.
+* sparseMode (parameter table: 0..8, 5 unsupported; constraint section:
+  modes 1, 2 and 3 ignore preTokens / nextTokens, modes 0 and 4 need the
+  attention mask to agree with the preTokens / nextTokens window, and modes
+  0, 2 and 3 are the lower-triangular mask cases).  The per-mode doc is not
+  on the page.  Readings: modes 0 and 4 are the preTokens / nextTokens
+  window; mode 2 is the lower-triangular mask aligned at the top-left corner
+  (j <= i); mode 3 is the lower-triangular mask aligned at the bottom-right
+  corner (j <= i + Lk - Lq).  Other modes are not modelled.
 * Outer split (the parameter table's qStartIdxOptional / kvStartIdxOptional:
   the global start index of this chunk's query / key-value sequence).  The
   window is evaluated on global positions: key j of the chunk is allowed
@@ -84,6 +92,21 @@ def mask_bit_offsets(lens_q, lens_kv, n_heads: int) -> np.ndarray:
     out = np.zeros(len(lq), dtype=np.int64)
     out[1:] = np.cumsum(per)[:-1]
     return out
+
+
+UNBOUNDED = 2 ** 31 - 1
+
+
+def mode_window(sparse_mode: int, pre_tokens: int, next_tokens: int, lq: int, lk: int):
+    """(pre, next) window of one sequence under the sparseMode readings of
+    the module docstring."""
+    if sparse_mode in (0, 4):
+        return pre_tokens, next_tokens
+    if sparse_mode == 2:
+        return UNBOUNDED, 0
+    if sparse_mode == 3:
+        return UNBOUNDED, lk - lq
+    raise ValueError(f"sparse mode {sparse_mode} is not modelled")
 
 
 def window_allowed(lq: int, lk: int, pre_tokens: int, next_tokens: int,
@@ -282,7 +305,7 @@ def _starts(starts, batch):
 
 
 def varlen_forward(q, k, v, lens_q, lens_kv, scale, pre_tokens, next_tokens,
-                   mask_u8=None, keep_prob=1.0, q_start=None, kv_start=None):
+                   mask_u8=None, keep_prob=1.0, q_start=None, kv_start=None, sparse_mode=0):
     """Forward over a packed batch: q [Tq, N, D], k/v [Tk, Nkv, D*].
     ``q_start`` / ``kv_start``: per-sequence global start indices of the
     chunks (outer split), or None for zeros.
@@ -304,10 +327,10 @@ def varlen_forward(q, k, v, lens_q, lens_kv, scale, pre_tokens, next_tokens,
         for n in range(n_heads):
             kv = n // group
             rows_fn, _ = _keep_fns(mask_u8, int(offs[b]) + n * lq * lk, lq, lk)
+            pre_b, next_b = mode_window(sparse_mode, pre_tokens, next_tokens, lq, lk)
             yb, mb, lb = unit_forward(q[cq[b]:cq[b + 1], n], k[ck[b]:ck[b + 1], kv],
-                                      v[ck[b]:ck[b + 1], kv], scale, pre_tokens,
-                                      next_tokens, rows_fn, keep_prob,
-                                      q_start=qs0[b], kv_start=ks0[b])
+                                      v[ck[b]:ck[b + 1], kv], scale, pre_b, next_b,
+                                      rows_fn, keep_prob, q_start=qs0[b], kv_start=ks0[b])
             y[cq[b]:cq[b + 1], n] = yb
             smax[cq[b]:cq[b + 1], n, :] = mb[:, None]
             ssum[cq[b]:cq[b + 1], n, :] = lb[:, None]
@@ -316,7 +339,7 @@ def varlen_forward(q, k, v, lens_q, lens_kv, scale, pre_tokens, next_tokens,
 
 def varlen_backward(q, k, v, dy, y, softmax_max, softmax_sum, lens_q, lens_kv,
                     scale, pre_tokens, next_tokens, mask_u8=None, keep_prob=1.0,
-                    q_start=None, kv_start=None):
+                    q_start=None, kv_start=None, sparse_mode=0):
     """Backward over a packed batch; reads lane 0 of the [T, N, 8] statistics.
     Returns dq [Tq, N, D], dk [Tk, Nkv, D], dv [Tk, Nkv, Dv] (grouped query
     heads add into their shared key/value head)."""
@@ -341,9 +364,10 @@ def varlen_backward(q, k, v, dy, y, softmax_max, softmax_sum, lens_q, lens_kv,
         for n in range(n_heads):
             kv = n // group
             rows_fn, _ = _keep_fns(mask_u8, int(offs[b]) + n * lq * lk, lq, lk)
+            pre_b, next_b = mode_window(sparse_mode, pre_tokens, next_tokens, lq, lk)
             dqb, dkb, dvb = unit_backward(q[qs, n], k[ks, kv], v[ks, kv], dy[qs, n],
                                           y[qs, n], smax[qs, n, 0], ssum[qs, n, 0],
-                                          scale, pre_tokens, next_tokens, rows_fn,
+                                          scale, pre_b, next_b, rows_fn,
                                           keep_prob, q_start=qs0[b], kv_start=ks0[b])
             dq[qs, n] = dqb
             dk[ks, kv] += dkb

@@ -430,3 +430,47 @@ def test_equal_starts_change_nothing():
                                   kv_start=[100, 7])
     for a, b in zip(base, moved):
         np.testing.assert_array_equal(a, b)
+
+
+# ---------------------------------------------------------------------------
+# sparseMode readings
+# ---------------------------------------------------------------------------
+
+def test_sparse_mode_fixture():
+    for c in _load("sparse_mode_cases.json")["cases"]:
+        pre_b, next_b = oracle.mode_window(c["mode"], c["pre"], c["next"], c["lq"], c["lk"])
+        got = oracle.window_allowed(c["lq"], c["lk"], pre_b, next_b)
+        assert got.astype(int).tolist() == c["allowed"], c
+
+
+def test_lower_triangular_modes_agree_on_square_sequences():
+    """For Lq = Lk the two lower-triangular modes and the causal window of
+    mode 0 are one mask, so every output agrees."""
+    rng = np.random.default_rng(14)
+    lens = [19, 33]
+    T = sum(lens)
+    q, k, v, dy = (rng.standard_normal((T, 2, 8)) for _ in range(4))
+    ref = oracle.varlen_forward(q, k, v, lens, lens, 0.3, 2 ** 31 - 1, 0)
+    gref = oracle.varlen_backward(q, k, v, dy, *ref, lens, lens, 0.3, 2 ** 31 - 1, 0)
+    for mode in (2, 3):
+        got = oracle.varlen_forward(q, k, v, lens, lens, 0.3, 5, 7, sparse_mode=mode)
+        for a, b in zip(got, ref):
+            np.testing.assert_array_equal(a, b)
+        g = oracle.varlen_backward(q, k, v, dy, *got, lens, lens, 0.3, 5, 7, sparse_mode=mode)
+        for a, b in zip(g, gref):
+            np.testing.assert_array_equal(a, b)
+
+
+def test_bottom_right_mode_is_the_top_left_mode_of_the_last_rows():
+    """Mode 3 on (Lq, Lk) with Lq <= Lk aligns the triangle at the last key:
+    it equals the top-left triangle of queries that start at global position
+    Lk - Lq, i.e. mode 2 with the outer-split start Lk - Lq."""
+    rng = np.random.default_rng(15)
+    lq, lk = 21, 50
+    q, dy = (rng.standard_normal((lq, 2, 8)) for _ in range(2))
+    k, v = (rng.standard_normal((lk, 2, 8)) for _ in range(2))
+    a = oracle.varlen_forward(q, k, v, [lq], [lk], 0.3, 0, 0, sparse_mode=3)
+    b = oracle.varlen_forward(q, k, v, [lq], [lk], 0.3, 0, 0, sparse_mode=2,
+                              q_start=[lk - lq], kv_start=[0])
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
