@@ -32,6 +32,13 @@
  *   Mask: key j is allowed for query i (0-based inside the sequence) iff
  *   i - pre_tokens <= j <= i + next_tokens (preTokens / nextTokens rows of
  *   the parameter table).  Causal = next_tokens 0, pre_tokens >= max length.
+ *   sparse_mode (parameter table row sparseMode; the page defers the
+ *   per-mode details to a document it does not include; these are the
+ *   readings): 0 and 4 = that window; 2 = lower triangle aligned at the
+ *   top-left corner, j <= i; 3 = lower triangle aligned at the bottom-right
+ *   corner, j <= i + Lk - Lq.  Modes 2 and 3 ignore pre_tokens / next_tokens
+ *   (constraint section).  The outer-split starts of the options structs
+ *   move the chosen window onto global positions.
  *   Grouped heads: query head n uses key/value head n / (head_num/head_num_kv)
  *   (constraint section: Nq/Nkv must be an integer).
  *
@@ -55,7 +62,8 @@
  *                      multiple of head_num_kv, unknown dtype, non-finite
  *                      scale, drop_mask_bytes too small
  *   FA_ERR_UNSUPPORTED a valid request this build does not implement:
- *                      head_dim not in {64, 128}, sparse_mode != 0
+ *                      head_dim not in {64, 128}, sparse_mode 1, 6, 7, 8
+ *                      (sparse_mode 5 or outside 0..8: FA_ERR_INVALID)
  *   FA_ERR_WORKSPACE   workspace_bytes below the size the size call gave
  *   FA_ERR_CUDA        a CUDA launch or copy failed
  *   FA_ERR_TIMEOUT     (fa_varlen_read_error only) a kernel's bounded wait

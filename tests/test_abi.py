@@ -85,6 +85,12 @@ def test_workspace_size_checks():
     assert _ws(lens_q=(1 << 20, 1))[0] == fa.FA_ERR_INVALID
     assert _ws(d=96)[0] == fa.FA_ERR_UNSUPPORTED
     assert _ws(sparse=1)[0] == fa.FA_ERR_UNSUPPORTED
+    for mode in (6, 7, 8):
+        assert _ws(sparse=mode)[0] == fa.FA_ERR_UNSUPPORTED
+    for mode in (-1, 5, 9):
+        assert _ws(sparse=mode)[0] == fa.FA_ERR_INVALID
+    for mode in (0, 2, 3, 4):
+        assert _ws(sparse=mode)[0] == fa.FA_OK
     assert _ws(lens_q=(0, 5, 0))[0] == fa.FA_OK
 
 
@@ -128,7 +134,8 @@ def test_bwd_argument_checks_before_any_launch():
     assert _bwd_call(scale=float("nan")) == fa.FA_ERR_INVALID
     assert _bwd_call(n=3, nkv=2) == fa.FA_ERR_INVALID
     assert _bwd_call(d=80) == fa.FA_ERR_UNSUPPORTED
-    assert _bwd_call(sparse=2) == fa.FA_ERR_UNSUPPORTED
+    assert _bwd_call(sparse=6) == fa.FA_ERR_UNSUPPORTED
+    assert _bwd_call(sparse=5) == fa.FA_ERR_INVALID
     assert _bwd_call(ws_bytes=16) == fa.FA_ERR_WORKSPACE
     assert _bwd_call(ws=None, ws_bytes=1 << 20) == fa.FA_ERR_NULLPTR
     assert _bwd_call(lens=(0,)) == fa.FA_OK                    # empty input: nothing to do

@@ -73,3 +73,42 @@ def test_query_chunks_reproduce_the_whole_sequence():
         dv_sum += dvc.float()
     assert rel_err(f64(dk_sum), f64(dk)) <= 1e-2
     assert rel_err(f64(dv_sum), f64(dv)) <= 1e-2
+
+
+MODE_CASES = {
+    # Lq < Lk, Lq > Lk and a zero-length sequence, for both lower-triangular modes
+    "mode2": (wl.Workload(64, "bf16", [100, 260, 0, 37], 2, 128, 3, 5, seed=25,
+                          lens_kv=[230, 140, 9, 37]), 2),
+    "mode3": (wl.Workload(65, "bf16", [100, 260, 0, 37], 2, 128, 3, 5, seed=26,
+                          lens_kv=[230, 140, 9, 37]), 3),
+    "mode3_gqa_dropout": (wl.Workload(66, "bf16", [150, 64], 4, 128, 0, 0, keep_prob=0.8,
+                                      seed=27, n_heads_kv=2, lens_kv=[300, 40]), 3),
+    "mode4_fp32": (wl.Workload(67, "fp32", [70, 33], 2, 64, 9, 2, seed=28,
+                               lens_kv=[50, 90]), 4),
+}
+
+
+@pytest.mark.parametrize("impl", ["simt", "tcgen05"])
+@pytest.mark.parametrize("name", list(MODE_CASES))
+def test_sparse_modes_against_oracle(name, impl):
+    w, mode = MODE_CASES[name]
+    if impl == "tcgen05" and (w.dtype == "fp32" or w.head_dim != 128):
+        pytest.skip("tcgen05 kernel not built for this case")
+    tensors = wl.make_tensors(w)
+    mask_np = wl.make_keep_mask(w)
+    mask = None if mask_np is None else torch.from_numpy(mask_np).to(DEV)
+    q, k, v, dy = (t.to(DEV) for t in tensors)
+    y, m, l = fa.fwd(q, k, v, w.lens, w.lens_kv, w.scale, w.pre_tokens, w.next_tokens,
+                     w.keep_prob, mask, sparse_mode=mode)
+    dq, dk, dv = fa.bwd(q, k, v, dy, y, m, l, w.lens, w.lens_kv, w.scale, w.pre_tokens,
+                        w.next_tokens, w.keep_prob, mask, impl=IMPLS[impl], sparse_mode=mode)
+    torch.cuda.synchronize()
+    qn, kn, vn, dyn = (f64(t) for t in tensors)
+    import oracle
+    ry, rm, rl = oracle.varlen_forward(qn, kn, vn, w.lens, w.lens_kv, w.scale, w.pre_tokens,
+                                       w.next_tokens, mask_np, w.keep_prob, sparse_mode=mode)
+    rdq, rdk, rdv = oracle.varlen_backward(qn, kn, vn, dyn, ry, rm, rl, w.lens, w.lens_kv,
+                                           w.scale, w.pre_tokens, w.next_tokens, mask_np,
+                                           w.keep_prob, sparse_mode=mode)
+    assert_close(dict(y=y, dq=dq, dk=dk, dv=dv), dict(y=ry, dq=rdq, dk=rdk, dv=rdv),
+                 TOL[w.dtype])

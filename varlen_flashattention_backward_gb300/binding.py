@@ -153,35 +153,39 @@ def _opts(impl=FA_BWD_AUTO, wait_timeout_ns=0, events=None, deterministic=False,
 
 
 def fwd_workspace_size(lens_q, lens_kv, n, n_kv, d, dtype, keep_prob=1.0,
-                       pre_tokens=2 ** 31 - 1, next_tokens=2 ** 31 - 1) -> int:
+                       pre_tokens=2 ** 31 - 1, next_tokens=2 ** 31 - 1, sparse_mode=0) -> int:
     lq, b, tq = _lens(lens_q)
     lk, _, tk = _lens(lens_kv)
     out = ctypes.c_size_t(0)
     _check(lib().fa_varlen_fwd_workspace_size(lq, lk, b, tq, tk, n, n_kv, d, _DTYPE[dtype], b"TND",
-                                              keep_prob, pre_tokens, next_tokens, 0,
-                                              ctypes.byref(out)), "fa_varlen_fwd_workspace_size")
+                                              keep_prob, pre_tokens, next_tokens,
+                                              int(sparse_mode), ctypes.byref(out)),
+           "fa_varlen_fwd_workspace_size")
     return out.value
 
 
 def bwd_workspace_size(lens_q, lens_kv, n, n_kv, d, dtype, keep_prob=1.0,
                        pre_tokens=2 ** 31 - 1, next_tokens=2 ** 31 - 1,
-                       impl=FA_BWD_AUTO) -> int:
+                       impl=FA_BWD_AUTO, sparse_mode=0) -> int:
     lq, b, tq = _lens(lens_q)
     lk, _, tk = _lens(lens_kv)
     out = ctypes.c_size_t(0)
     opt = _opts(impl)
     _check(lib().fa_varlen_bwd_workspace_size_ex(lq, lk, b, tq, tk, n, n_kv, d, _DTYPE[dtype],
-                                                 b"TND", keep_prob, pre_tokens, next_tokens, 0,
-                                                 ctypes.byref(opt), ctypes.byref(out)),
+                                                 b"TND", keep_prob, pre_tokens, next_tokens,
+                                                 int(sparse_mode), ctypes.byref(opt),
+                                                 ctypes.byref(out)),
            "fa_varlen_bwd_workspace_size_ex")
     return out.value
 
 
 def fwd(q, k, v, lens_q, lens_kv, scale, pre_tokens, next_tokens, keep_prob=1.0,
         drop_mask=None, y=None, softmax_max=None, softmax_sum=None, workspace=None,
-        stream=None, q_start=None, kv_start=None):
+        stream=None, q_start=None, kv_start=None, sparse_mode=0):
     """Y and the [T, N, 8] statistics (fa_varlen_fwd_ex).  ``q_start`` /
-    ``kv_start``: per-sequence global chunk starts (outer split), or None."""
+    ``kv_start``: per-sequence global chunk starts (outer split), or None.
+    ``sparse_mode``: 0 or 4 (preTokens / nextTokens band), 2 (lower triangle
+    from the top-left corner), 3 (lower triangle from the bottom-right)."""
     tq, n, d = q.shape
     n_kv = k.shape[1]
     lq, b, _ = _lens(lens_q)
@@ -195,7 +199,7 @@ def fwd(q, k, v, lens_q, lens_kv, scale, pre_tokens, next_tokens, keep_prob=1.0,
         softmax_sum = torch.empty(tq, n, 8, dtype=torch.float32, device=dev)
     if workspace is None:
         ws = fwd_workspace_size(lens_q, lens_kv, n, n_kv, d, q.dtype, keep_prob, pre_tokens,
-                                next_tokens)
+                                next_tokens, sparse_mode)
         workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
     mask_bytes = 0 if drop_mask is None else drop_mask.numel()
     qs, ks = _starts(q_start), _starts(kv_start)
@@ -204,7 +208,7 @@ def fwd(q, k, v, lens_q, lens_kv, scale, pre_tokens, next_tokens, keep_prob=1.0,
     _check(lib().fa_varlen_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(drop_mask), mask_bytes, lq, lk,
                                   b, tq, k.shape[0], n, n_kv, d, _DTYPE[q.dtype], b"TND",
                                   float(scale), float(keep_prob), int(pre_tokens),
-                                  int(next_tokens), 0, _ptr(y), _ptr(softmax_max),
+                                  int(next_tokens), int(sparse_mode), _ptr(y), _ptr(softmax_max),
                                   _ptr(softmax_sum), _ptr(workspace), workspace.numel(),
                                   _stream(stream), ctypes.byref(opt)), "fa_varlen_fwd_ex")
     return y, softmax_max, softmax_sum
@@ -213,11 +217,12 @@ def fwd(q, k, v, lens_q, lens_kv, scale, pre_tokens, next_tokens, keep_prob=1.0,
 def bwd(q, k, v, dy, y, softmax_max, softmax_sum, lens_q, lens_kv, scale, pre_tokens,
         next_tokens, keep_prob=1.0, drop_mask=None, dq=None, dk=None, dv=None,
         workspace=None, stream=None, impl=FA_BWD_AUTO, wait_timeout_ns=0, events=None,
-        deterministic=False, q_start=None, kv_start=None):
+        deterministic=False, q_start=None, kv_start=None, sparse_mode=0):
     """dQ, dK, dV (fa_varlen_bwd_ex).  ``events``: four torch.cuda.Event
     (already recorded once, so that they exist) recorded around the kernels.
     ``deterministic``: add the dQ partials in a fixed order (bitwise
-    reproducible dQ)."""
+    reproducible dQ).  ``q_start`` / ``kv_start`` / ``sparse_mode``: as in
+    ``fwd`` (give the forward the same values)."""
     tq, n, d = q.shape
     n_kv = k.shape[1]
     lq, b, _ = _lens(lens_q)
@@ -230,7 +235,7 @@ def bwd(q, k, v, dy, y, softmax_max, softmax_sum, lens_q, lens_kv, scale, pre_to
         dv = torch.empty_like(v)
     if workspace is None:
         ws = bwd_workspace_size(lens_q, lens_kv, n, n_kv, d, q.dtype, keep_prob, pre_tokens,
-                                next_tokens, impl)
+                                next_tokens, impl, sparse_mode)
         workspace = torch.empty(ws, dtype=torch.uint8, device=q.device)
     mask_bytes = 0 if drop_mask is None else drop_mask.numel()
     opt = _opts(impl, wait_timeout_ns, events, deterministic, q_start, kv_start)
@@ -238,7 +243,8 @@ def bwd(q, k, v, dy, y, softmax_max, softmax_sum, lens_q, lens_kv, scale, pre_to
                                   mask_bytes, _ptr(softmax_max), _ptr(softmax_sum), _ptr(y), lq,
                                   lk, b, tq, k.shape[0], n, n_kv, d, _DTYPE[q.dtype], b"TND",
                                   float(scale), float(keep_prob), int(pre_tokens),
-                                  int(next_tokens), 0, _ptr(dq), _ptr(dk), _ptr(dv),
+                                  int(next_tokens), int(sparse_mode), _ptr(dq), _ptr(dk),
+                                  _ptr(dv),
                                   _ptr(workspace), workspace.numel(), _stream(stream),
                                   ctypes.byref(opt)), "fa_varlen_bwd_ex")
     return dq, dk, dv

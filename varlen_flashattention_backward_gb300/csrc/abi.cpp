@@ -44,12 +44,25 @@ struct Problem {
   // (host arrays of length batch), or null for 0.
   const int64_t *q_start = nullptr, *kv_start = nullptr;
 
-  // Window of sequence b on chunk-local indices (see SeqInfo::pre).
+  // Window of sequence b on chunk-local indices (see SeqInfo::pre).  The
+  // sparse mode picks the window on global positions (modes 0 and 4: the
+  // preTokens / nextTokens band; 2: lower triangle aligned at the top-left
+  // corner; 3: lower triangle aligned at the bottom-right corner, j <= i +
+  // Lk - Lq; modes 1-3 ignore preTokens / nextTokens), then the chunk starts
+  // shift it onto chunk-local indices.
   int64_t shift(int64_t b) const {
     return (q_start ? q_start[b] : 0) - (kv_start ? kv_start[b] : 0);
   }
-  int64_t pre_of(int64_t b) const { return clamp_window(clamp_window(pre) - shift(b)); }
-  int64_t next_of(int64_t b) const { return clamp_window(clamp_window(next) + shift(b)); }
+  int64_t mode_pre(int64_t) const {
+    return (sparse_mode == 2 || sparse_mode == 3) ? (int64_t(1) << 28) : clamp_window(pre);
+  }
+  int64_t mode_next(int64_t b) const {
+    if (sparse_mode == 2) return 0;
+    if (sparse_mode == 3) return lens_kv[b] - lens_q[b];
+    return clamp_window(next);
+  }
+  int64_t pre_of(int64_t b) const { return clamp_window(mode_pre(b) - shift(b)); }
+  int64_t next_of(int64_t b) const { return clamp_window(mode_next(b) + shift(b)); }
 };
 
 // Checks shared by every entry point.  `need_ptrs` lists pointers that must
@@ -82,7 +95,10 @@ fa_status check_problem(Problem &pr, const char *layout,
   for (int64_t b = 0; b < pr.batch; ++b)
     if ((pr.q_start && pr.q_start[b] < 0) || (pr.kv_start && pr.kv_start[b] < 0))
       return FA_ERR_INVALID;
-  if (pr.sparse_mode != 0) return FA_ERR_UNSUPPORTED;
+  // sparseMode: 0..8, 5 not supported (parameter table); this build
+  // implements the window modes 0, 2, 3 and 4.
+  if (pr.sparse_mode < 0 || pr.sparse_mode > 8 || pr.sparse_mode == 5) return FA_ERR_INVALID;
+  if (pr.sparse_mode == 1 || pr.sparse_mode > 4) return FA_ERR_UNSUPPORTED;
   if (pr.d != 64 && pr.d != 128) return FA_ERR_UNSUPPORTED;
   pr.tp = tp;
   pr.mask_bits = bits;
@@ -201,12 +217,15 @@ int64_t count_items(const Problem &pr, int tile, bool fwd) {
   return c;
 }
 
-// First key tile visiting each padded query tile (the deterministic mode's
-// order base).  The key tiles that visit one query tile form a contiguous
-// range for every window, because both ends of a key tile's query range grow
-// with the tile index; the check below guards that property.
-bool build_qfirst(const Problem &pr, const std::vector<SeqInfo> &seqs,
-                  const std::vector<WorkItem> &items, std::vector<int32_t> &qfirst) {
+// Per padded query tile: the first key tile visiting it (the deterministic
+// mode's order base) and the number of key tiles visiting it, stored as
+// [qfirst | qcount].  The key tiles that visit
+// one query tile form a contiguous range for every window, because both ends
+// of a key tile's query range grow with the tile index; `contiguous` reports
+// that property, which the deterministic mode relies on.
+void build_qtables(const Problem &pr, const std::vector<SeqInfo> &seqs,
+                   const std::vector<WorkItem> &items, std::vector<int32_t> &tab,
+                   bool *contiguous) {
   const size_t g_tiles = size_t(pr.tp / kQTile);
   std::vector<int32_t> lo(g_tiles, INT32_MAX), hi(g_tiles, -1), cnt(g_tiles, 0);
   for (const WorkItem &w : items) {
@@ -218,13 +237,14 @@ bool build_qfirst(const Problem &pr, const std::vector<SeqInfo> &seqs,
       ++cnt[g0 + t];
     }
   }
-  qfirst.assign(g_tiles, 0);
+  tab.assign(2 * g_tiles, 0);
+  *contiguous = true;
   for (size_t g = 0; g < g_tiles; ++g) {
+    tab[g_tiles + g] = cnt[g];
     if (cnt[g] == 0) continue;
-    if (hi[g] - lo[g] + 1 != cnt[g]) return false;
-    qfirst[g] = lo[g];
+    if (hi[g] - lo[g] + 1 != cnt[g]) *contiguous = false;
+    tab[g] = lo[g];
   }
-  return true;
 }
 
 struct BwdLayout {
@@ -249,8 +269,8 @@ BwdLayout bwd_layout(const Problem &pr, int impl) {
   off = align_up(off + sizeof(SeqInfo) * size_t(pr.batch));
   L.items = off;
   off = align_up(off + sizeof(WorkItem) * size_t(count_items(pr, tile, false)));
-  L.qfirst = off;
-  off = align_up(off + sizeof(int32_t) * size_t(pr.tp / kQTile));
+  L.qfirst = off;   // [qfirst | qcount]
+  off = align_up(off + 2 * sizeof(int32_t) * size_t(pr.tp / kQTile));
   L.lse = off;
   off = align_up(off + sizeof(float) * size_t(pr.n * pr.tp));
   L.dsum = off;
@@ -311,7 +331,8 @@ const char *fa_status_string(fa_status s) {
     case FA_OK: return "FA_OK";
     case FA_ERR_NULLPTR: return "FA_ERR_NULLPTR: a required pointer is null";
     case FA_ERR_INVALID: return "FA_ERR_INVALID: an argument is out of range";
-    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: valid request not implemented by this build";
+    case FA_ERR_UNSUPPORTED:
+      return "FA_ERR_UNSUPPORTED: valid request not implemented by this build";
     case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace too small";
     case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call failed";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a bounded in-kernel wait expired";
@@ -495,9 +516,13 @@ fa_status fa_varlen_bwd_ex(const void *q, const void *k, const void *v, const vo
   const bool det = options && options->deterministic != 0;
   auto seqs = build_seqs(pr);
   auto items = build_bwd_items(pr, tile, det);
-  std::vector<int32_t> qfirst;
-  if (det && !build_qfirst(pr, seqs, items, qfirst)) return FA_ERR_UNSUPPORTED;
-  st = upload_plan(workspace, L.seqs, L.items, seqs, items, cs, L.qfirst, det ? &qfirst : nullptr);
+  std::vector<int32_t> qtab;
+  if (det) {
+    bool contiguous = true;
+    build_qtables(pr, seqs, items, qtab, &contiguous);
+    if (!contiguous) return FA_ERR_UNSUPPORTED;
+  }
+  st = upload_plan(workspace, L.seqs, L.items, seqs, items, cs, L.qfirst, det ? &qtab : nullptr);
   if (st != FA_OK) return st;
 
   uint8_t *ws = static_cast<uint8_t *>(workspace);

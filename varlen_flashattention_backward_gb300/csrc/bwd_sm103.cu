@@ -116,7 +116,8 @@ __device__ __forceinline__ uint32_t fetch_bits32(const uint8_t *mask, int64_t nb
     uint64_t w = 0;
     for (int k = 0; k < 8; ++k) {
       const uintptr_t a = al + k;
-      if (a >= base && a < end) w |= uint64_t(__ldg(reinterpret_cast<const uint8_t *>(a))) << (8 * k);
+      if (a >= base && a < end)
+        w |= uint64_t(__ldg(reinterpret_cast<const uint8_t *>(a))) << (8 * k);
     }
     lo = uint32_t(w);
     hi = uint32_t(w >> 32);
@@ -403,8 +404,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 l4 = ld_shared_f4(lse_addr + 16 * c4);
-          fma2(pr[4 * c4], pr[4 * c4 + 1], __uint_as_float(r[4 * c4]), __uint_as_float(r[4 * c4 + 1]), sl2, sl2, -l4.x, -l4.y);
-          fma2(pr[4 * c4 + 2], pr[4 * c4 + 3], __uint_as_float(r[4 * c4 + 2]), __uint_as_float(r[4 * c4 + 3]), sl2, sl2, -l4.z, -l4.w);
+          fma2(pr[4 * c4], pr[4 * c4 + 1], __uint_as_float(r[4 * c4]),
+               __uint_as_float(r[4 * c4 + 1]), sl2, sl2, -l4.x, -l4.y);
+          fma2(pr[4 * c4 + 2], pr[4 * c4 + 3], __uint_as_float(r[4 * c4 + 2]),
+               __uint_as_float(r[4 * c4 + 3]), sl2, sl2, -l4.z, -l4.w);
           pr[4 * c4 + 0] = ex2(pr[4 * c4 + 0]);
           pr[4 * c4 + 1] = ex2(pr[4 * c4 + 1]);
           pr[4 * c4 + 2] = ex2(pr[4 * c4 + 2]);
@@ -468,8 +471,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               ds[e] = pr[c] * (__uint_as_float(rdp[c]) * z - dv[e]);
             }
           } else {
-            sub2(ds[0], ds[1], __uint_as_float(rdp[4 * c4]), __uint_as_float(rdp[4 * c4 + 1]), dv[0], dv[1]);
-            sub2(ds[2], ds[3], __uint_as_float(rdp[4 * c4 + 2]), __uint_as_float(rdp[4 * c4 + 3]), dv[2], dv[3]);
+            sub2(ds[0], ds[1], __uint_as_float(rdp[4 * c4]), __uint_as_float(rdp[4 * c4 + 1]),
+                 dv[0], dv[1]);
+            sub2(ds[2], ds[3], __uint_as_float(rdp[4 * c4 + 2]),
+                 __uint_as_float(rdp[4 * c4 + 3]), dv[2], dv[3]);
             mul2(ds[0], ds[1], ds[0], ds[1], pr[4 * c4], pr[4 * c4 + 1]);
             mul2(ds[2], ds[3], ds[2], ds[3], pr[4 * c4 + 2], pr[4 * c4 + 3]);
           }
@@ -693,8 +698,10 @@ bool tcgen05_supported(fa_dtype dt, int head_dim) {
 }
 
 cudaError_t launch_bwd_tcgen05(const BwdParams &p, fa_dtype dt, cudaStream_t s) {
-  if (dt == FA_DTYPE_BF16) return p.deterministic ? launch_t<true, true>(p, s) : launch_t<true, false>(p, s);
-  if (dt == FA_DTYPE_FP16) return p.deterministic ? launch_t<false, true>(p, s) : launch_t<false, false>(p, s);
+  if (dt == FA_DTYPE_BF16)
+    return p.deterministic ? launch_t<true, true>(p, s) : launch_t<true, false>(p, s);
+  if (dt == FA_DTYPE_FP16)
+    return p.deterministic ? launch_t<false, true>(p, s) : launch_t<false, false>(p, s);
   return cudaErrorInvalidValue;
 }
 
