@@ -499,10 +499,12 @@ fa_status fa_varlen_bwd_ex(const void *q, const void *k, const void *v, const vo
   if (impl == FA_BWD_TCGEN05 && !tcgen05_supported(dtype, int(head_dim)))
     return FA_ERR_UNSUPPORTED;
   if (total_q == 0 && total_kv == 0) return FA_OK;
-  // The tensor-core kernel reads q, k, v, dy through TMA, which needs 16-byte
-  // aligned bases; with no query rows there is nothing for it to do.
+  // The tensor-core kernel reads q, k, v, dy and writes dk, dv through TMA,
+  // which needs 16-byte aligned bases; with no query rows there is nothing
+  // for it to do.
   const auto al16 = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; };
-  const bool tma_ok = total_q > 0 && al16(q) && al16(k) && al16(v) && al16(dy);
+  const bool tma_ok =
+      total_q > 0 && al16(q) && al16(k) && al16(v) && al16(dy) && al16(dk) && al16(dv);
   if (impl == FA_BWD_TCGEN05 && !tma_ok) {
     if (options && options->impl == FA_BWD_TCGEN05 && total_q > 0) return FA_ERR_UNSUPPORTED;
     impl = FA_BWD_SIMT;

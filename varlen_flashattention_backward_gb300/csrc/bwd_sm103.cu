@@ -86,7 +86,7 @@ static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 enum : int {
   B_KV = 0, B_FULL = 1, B_EMPTY = B_FULL + STAGES, B_SDFULL = B_EMPTY + STAGES, B_SDFREE,
   B_PFULL, B_PFREE, B_DSFULL, B_DSFREE, B_DQFULL, B_DQFREE, B_ACC, B_FINAL, B_FINAL_A,
-  B_COUNT
+  B_EPI, B_COUNT = B_EPI + 2
 };
 static_assert(B_COUNT * 8 <= 256, "barrier area");
 
@@ -97,6 +97,7 @@ enum : int {
 
 struct TcMaps {
   CUtensorMap q, dy, k, v;
+  CUtensorMap dk, dv;   // same shape as k / v, for the epilogue's bulk stores
 };
 
 // Bits [bit, bit + 32) of the keep mask, read without leaving
@@ -168,6 +169,7 @@ __device__ __forceinline__ void drain_bar_sync() {
   asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
+
 struct Ctl {
   int *abort;         // shared-memory flag: some wait of this CTA gave up
   int32_t *err;       // global error word
@@ -227,6 +229,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(bar(B_ACC), 1);
     mbar_init(bar(B_FINAL), 1);
     mbar_init(bar(B_FINAL_A), 1);
+    mbar_init(bar(B_EPI), 4);       // epilogue: the four warps of the dV half
+    mbar_init(bar(B_EPI + 1), 4);   // ... and of the dK half
     mbar_fence_init();
   }
   if (warp == 1) {
@@ -262,6 +266,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tma_load_2d_w(sb + SM_K + 16384, &maps.k, bar(B_KV), kx + 64, ky);
       tma_load_2d_w(sb + SM_V, &maps.v, bar(B_KV), kx, ky);
       tma_load_2d_w(sb + SM_V + 16384, &maps.v, bar(B_KV), kx + 64, ky);
+      // The item `prefetch_ahead` places further down the list starts on
+      // some SM about when this one ends: bring its K and V into L2 now.
+      if (lane == 0 && blockIdx.x + p.prefetch_ahead < p.n_items) {
+        const WorkItem nx = p.items[blockIdx.x + p.prefetch_ahead];
+        const int nky = p.seqs[nx.seq].cu_k + nx.tile * BN, nkx = nx.head * HD;
+        tma_prefetch_l2_2d(&maps.k, nkx, nky);
+        tma_prefetch_l2_2d(&maps.k, nkx + 64, nky);
+        tma_prefetch_l2_2d(&maps.v, nkx, nky);
+        tma_prefetch_l2_2d(&maps.v, nkx + 64, nky);
+      }
+      __syncwarp();
       int issued = 0;
       for (int L = 0; L < n_it; ++L) {
         const int st = L % STAGES;
@@ -501,7 +516,53 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     bool have = n_it > 0 && !*reinterpret_cast<volatile int *>(&s_abort);
     if (have) have = wait_or_abort(ctl, bar(B_ACC), 0, ROLE_EPILOGUE);
     tc_fence_after();
-    if (n_it == 0 || have) {
+    // A full key tile goes out through shared memory and two bulk tensor
+    // stores per tensor (dV staged in the idle Q stages, dK in the dY
+    // stages, as two [128 x 64] boxes in the 128-byte swizzle); the last,
+    // partial tile of a sequence is stored row by row, so that no row of
+    // the next sequence is touched.
+    const bool tile_full = k0 + BN <= sq.len_k;
+    if (tile_full && (n_it == 0 || have)) {
+      const float sc = half == 0 ? 1.f : p.scale;
+      const uint32_t col = half == 0 ? COL_DV : COL_DK;
+      const uint32_t stage = sb + (half == 0 ? SM_Q : SM_DY);
+#pragma unroll 1
+      for (int c0 = 0; c0 < HD; c0 += 32) {
+        uint32_t r[32];
+        if (n_it > 0) {
+          tmem_ld32(tmem + lane_off + col + c0, r);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = 0u;
+        }
+        // columns c0 .. c0 + 31 = 16-byte chunks (c0 % 64) / 8 .. + 3 of box c0 / 64
+        const uint32_t rowa = stage + uint32_t(c0 / 64) * 16384u + uint32_t(jl) * 128u;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[e] = pack2<kBF16>(__uint_as_float(r[8 * v + 2 * e]) * sc,
+                                __uint_as_float(r[8 * v + 2 * e + 1]) * sc);
+          const uint32_t chunk = uint32_t(((c0 % 64) / 8 + v) ^ (jl & 7));
+          st_shared_v4(rowa + chunk * 16u, w[0], w[1], w[2], w[3]);
+        }
+      }
+      // The four warps of this half report their rows (bounded wait, so that
+      // a warp that gave up cannot hold the others), then one thread stores.
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_EPI + half));
+      if (quarter == 0 && lane == 0 &&
+          wait_or_abort(ctl, bar(B_EPI + half), 0, ROLE_EPILOGUE)) {
+        const CUtensorMap *m = half == 0 ? &maps.dv : &maps.dk;
+        const int y = sq.cu_k + k0, x = kvh * HD;
+        tma_store_2d(m, stage, x, y);
+        tma_store_2d(m, stage + 16384, x + 64, y);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+      }
+    } else if (n_it == 0 || have) {
       using T = typename std::conditional<kBF16, __nv_bfloat16, __half>::type;
       T *out = static_cast<T *>(half == 0 ? p.dv : p.dk);
       const float sc = half == 0 ? 1.f : p.scale;
@@ -675,12 +736,20 @@ cudaError_t launch_t(const BwdParams &p, cudaStream_t st) {
   if (!make_map(&maps.q, p.q, p.total_q, p.n, BM, kBF16) ||
       !make_map(&maps.dy, p.dy, p.total_q, p.n, BM, kBF16) ||
       !make_map(&maps.k, p.k, p.total_kv, p.n_kv, BN, kBF16) ||
-      !make_map(&maps.v, p.v, p.total_kv, p.n_kv, BN, kBF16))
+      !make_map(&maps.v, p.v, p.total_kv, p.n_kv, BN, kBF16) ||
+      !make_map(&maps.dk, p.dk, p.total_kv, p.n_kv, BN, kBF16) ||
+      !make_map(&maps.dv, p.dv, p.total_kv, p.n_kv, BN, kBF16))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<kBF16, kDet>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  bwd_tc_kernel<kBF16, kDet><<<p.n_items, NTHREADS, SMEM_BYTES, st>>>(p, maps);
+  int dev = 0;
+  BwdParams q = p;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&q.prefetch_ahead, cudaDevAttrMultiProcessorCount, dev)) !=
+      cudaSuccess)
+    return e;
+  bwd_tc_kernel<kBF16, kDet><<<p.n_items, NTHREADS, SMEM_BYTES, st>>>(q, maps);
   return cudaGetLastError();
 }
 

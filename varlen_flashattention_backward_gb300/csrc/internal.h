@@ -77,6 +77,7 @@ struct BwdParams {
   int32_t *sem;
   const int32_t *qfirst;
   int n_items, batch, n, n_kv, d, tp, total_q, total_kv;
+  int prefetch_ahead;   // tcgen05 kernel: item distance of the K/V L2 prefetch (the SM count)
   float scale, scale_log2, inv_keep;
   int use_dropout;
   long long timeout_ns;
