@@ -55,6 +55,12 @@ Readings taken where the page is silent or ambiguous:
   window; mode 2 is the lower-triangular mask aligned at the top-left corner
   (j <= i); mode 3 is the lower-triangular mask aligned at the bottom-right
   corner (j <= i + Lk - Lq).  Other modes are not modelled.
+* attenMaskOptional (parameter table: 1 = the position does not take part,
+  0 = it does; shapes [B,N,Sq,Skv] ... [Sq,Skv]).  Reading: one [Sq, Skv]
+  matrix shared by every sequence and head, indexed by the chunk-local
+  (i, j) of each sequence; sparseMode 1 applies it alone (no window), modes
+  0 and 4 apply it together with the preTokens / nextTokens window (the
+  constraint section asks the two to agree), modes 2 and 3 do not read it.
 * Outer split (the parameter table's qStartIdxOptional / kvStartIdxOptional:
   the global start index of this chunk's query / key-value sequence).  The
   window is evaluated on global positions: key j of the chunk is allowed
@@ -102,6 +108,8 @@ def mode_window(sparse_mode: int, pre_tokens: int, next_tokens: int, lq: int, lk
     the module docstring."""
     if sparse_mode in (0, 4):
         return pre_tokens, next_tokens
+    if sparse_mode == 1:
+        return UNBOUNDED, UNBOUNDED
     if sparse_mode == 2:
         return UNBOUNDED, 0
     if sparse_mode == 3:
@@ -174,7 +182,7 @@ def _zscale(keep_rows, r0, r1, lk, keep_prob):
 
 
 def unit_forward(q, k, v, scale, pre_tokens, next_tokens, keep_rows=None,
-                 keep_prob=1.0, block=ROW_BLOCK, q_start=0, kv_start=0):
+                 keep_prob=1.0, block=ROW_BLOCK, q_start=0, kv_start=0, masked=None):
     """Y = Dropout(Softmax(S), keep_prob) V for one unit, plus the softmax
     statistics (max, sum) the forward hands to the backward.
 
@@ -189,6 +197,8 @@ def unit_forward(q, k, v, scale, pre_tokens, next_tokens, keep_rows=None,
         r1 = min(lq, r0 + block)
         allowed = window_allowed(lq, lk, pre_tokens, next_tokens, np.arange(r0, r1),
                                  q_start, kv_start)
+        if masked is not None:
+            allowed &= ~masked[r0:r1]
         s = unit_logits(q[r0:r1], k, scale, allowed)
         mb, lb = _softmax_stats(s)
         p = _probs(s, mb, lb)
@@ -201,7 +211,7 @@ def unit_forward(q, k, v, scale, pre_tokens, next_tokens, keep_rows=None,
 
 def unit_backward(q, k, v, dy, y, m, l, scale, pre_tokens, next_tokens,
                   keep_rows=None, keep_prob=1.0, block=ROW_BLOCK,
-                  return_ds=False, q_start=0, kv_start=0):
+                  return_ds=False, q_start=0, kv_start=0, masked=None):
     """dQ, dK, dV of one unit from the backward formulas, using the given
     forward output ``y`` (attentionIn) and statistics ``m``/``l``.
 
@@ -222,6 +232,8 @@ def unit_backward(q, k, v, dy, y, m, l, scale, pre_tokens, next_tokens,
         r1 = min(lq, r0 + block)
         allowed = window_allowed(lq, lk, pre_tokens, next_tokens, np.arange(r0, r1),
                                  q_start, kv_start)
+        if masked is not None:
+            allowed &= ~masked[r0:r1]
         s = unit_logits(q[r0:r1], k, scale, allowed)
         p = _probs(s, m[r0:r1], l[r0:r1])
         z = _zscale(keep_rows, r0, r1, lk, keep_prob)
@@ -238,7 +250,8 @@ def unit_backward(q, k, v, dy, y, m, l, scale, pre_tokens, next_tokens,
 
 
 def unit_backward_rows(rows, q, k, v, dy, y, m, l, scale, pre_tokens,
-                       next_tokens, keep_rows=None, keep_prob=1.0, q_start=0, kv_start=0):
+                       next_tokens, keep_rows=None, keep_prob=1.0, q_start=0, kv_start=0,
+                       masked=None):
     """dQ at the given query rows only (each row of dS needs only its own
     row of S, dP and D)."""
     rows = np.asarray(rows, dtype=np.int64)
@@ -247,6 +260,8 @@ def unit_backward_rows(rows, q, k, v, dy, y, m, l, scale, pre_tokens,
     y = np.asarray(y, np.float64)
     lq, lk = q.shape[0], k.shape[0]
     allowed = window_allowed(lq, lk, pre_tokens, next_tokens, rows, q_start, kv_start)
+    if masked is not None:
+        allowed &= ~masked[rows]
     s = unit_logits(q[rows], k, scale, allowed)
     p = _probs(s, np.asarray(m, np.float64)[rows], np.asarray(l, np.float64)[rows])
     if keep_rows is None or keep_prob >= 1.0:
@@ -260,7 +275,8 @@ def unit_backward_rows(rows, q, k, v, dy, y, m, l, scale, pre_tokens,
 
 
 def unit_backward_cols(cols, q, k, v, dy, y, m, l, scale, pre_tokens,
-                       next_tokens, keep_cols=None, keep_prob=1.0, q_start=0, kv_start=0):
+                       next_tokens, keep_cols=None, keep_prob=1.0, q_start=0, kv_start=0,
+                       masked=None):
     """dK and dV at the given key rows only (column j of P and dS runs over
     every query row i, so the full statistics m, l and D are used).
 
@@ -274,6 +290,8 @@ def unit_backward_cols(cols, q, k, v, dy, y, m, l, scale, pre_tokens,
     i = np.arange(lq, dtype=np.int64)[:, None] + int(q_start)
     j = cols[None, :] + int(kv_start)
     allowed = (j >= i - pre_tokens) & (j <= i + next_tokens)
+    if masked is not None:
+        allowed &= ~masked[:, cols]
     s = np.where(allowed, scale * (q @ k[cols].T), -np.inf)
     p = _probs(s, m, l)
     if keep_cols is None or keep_prob >= 1.0:
@@ -300,12 +318,21 @@ def _keep_fns(mask_u8, bit_off, lq, lk):
     return rows_fn, cols_fn
 
 
+def _unit_mask(atten_mask, sparse_mode, lq, lk):
+    """The attention mask's [lq, lk] corner as booleans (True = masked out),
+    or None where the mode does not read it."""
+    if atten_mask is None or sparse_mode not in (0, 1, 4):
+        return None
+    return np.asarray(atten_mask)[:lq, :lk] != 0
+
+
 def _starts(starts, batch):
     return [0] * batch if starts is None else [int(x) for x in starts]
 
 
 def varlen_forward(q, k, v, lens_q, lens_kv, scale, pre_tokens, next_tokens,
-                   mask_u8=None, keep_prob=1.0, q_start=None, kv_start=None, sparse_mode=0):
+                   mask_u8=None, keep_prob=1.0, q_start=None, kv_start=None, sparse_mode=0,
+                   atten_mask=None):
     """Forward over a packed batch: q [Tq, N, D], k/v [Tk, Nkv, D*].
     ``q_start`` / ``kv_start``: per-sequence global start indices of the
     chunks (outer split), or None for zeros.
@@ -330,7 +357,8 @@ def varlen_forward(q, k, v, lens_q, lens_kv, scale, pre_tokens, next_tokens,
             pre_b, next_b = mode_window(sparse_mode, pre_tokens, next_tokens, lq, lk)
             yb, mb, lb = unit_forward(q[cq[b]:cq[b + 1], n], k[ck[b]:ck[b + 1], kv],
                                       v[ck[b]:ck[b + 1], kv], scale, pre_b, next_b,
-                                      rows_fn, keep_prob, q_start=qs0[b], kv_start=ks0[b])
+                                      rows_fn, keep_prob, q_start=qs0[b], kv_start=ks0[b],
+                                      masked=_unit_mask(atten_mask, sparse_mode, lq, lk))
             y[cq[b]:cq[b + 1], n] = yb
             smax[cq[b]:cq[b + 1], n, :] = mb[:, None]
             ssum[cq[b]:cq[b + 1], n, :] = lb[:, None]
@@ -339,7 +367,7 @@ def varlen_forward(q, k, v, lens_q, lens_kv, scale, pre_tokens, next_tokens,
 
 def varlen_backward(q, k, v, dy, y, softmax_max, softmax_sum, lens_q, lens_kv,
                     scale, pre_tokens, next_tokens, mask_u8=None, keep_prob=1.0,
-                    q_start=None, kv_start=None, sparse_mode=0):
+                    q_start=None, kv_start=None, sparse_mode=0, atten_mask=None):
     """Backward over a packed batch; reads lane 0 of the [T, N, 8] statistics.
     Returns dq [Tq, N, D], dk [Tk, Nkv, D], dv [Tk, Nkv, Dv] (grouped query
     heads add into their shared key/value head)."""
@@ -368,7 +396,8 @@ def varlen_backward(q, k, v, dy, y, softmax_max, softmax_sum, lens_q, lens_kv,
             dqb, dkb, dvb = unit_backward(q[qs, n], k[ks, kv], v[ks, kv], dy[qs, n],
                                           y[qs, n], smax[qs, n, 0], ssum[qs, n, 0],
                                           scale, pre_b, next_b, rows_fn,
-                                          keep_prob, q_start=qs0[b], kv_start=ks0[b])
+                                          keep_prob, q_start=qs0[b], kv_start=ks0[b],
+                                          masked=_unit_mask(atten_mask, sparse_mode, lq, lk))
             dq[qs, n] = dqb
             dk[ks, kv] += dkb
             dv[ks, kv] += dvb

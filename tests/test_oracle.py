@@ -474,3 +474,84 @@ def test_bottom_right_mode_is_the_top_left_mode_of_the_last_rows():
                               q_start=[lk - lq], kv_start=[0])
     for x, y in zip(a, b):
         np.testing.assert_array_equal(x, y)
+
+
+# ---------------------------------------------------------------------------
+# explicit attention mask
+# ---------------------------------------------------------------------------
+
+def test_atten_mask_fixture_through_uniform_attention():
+    """With Q = 0 every allowed key gets the same weight, and with one-hot
+    value rows Y_i is 1/|allowed_i| on the allowed keys and 0 elsewhere (0
+    for a row with no allowed key): the forward's output spells out the
+    allowed set, which must match the hand-enumerated matrix."""
+    g = _load("atten_mask_cases.json")
+    mask = np.array(g["mask"], np.uint8)
+    for c in g["cases"]:
+        lq, lk = c["lq"], c["lk"]
+        q = np.zeros((lq, 1, 8))
+        k = np.random.default_rng(1).standard_normal((lk, 1, 8))
+        v = np.zeros((lk, 1, 8))
+        v[np.arange(lk), 0, np.arange(lk)] = 1.0
+        y, m, l = oracle.varlen_forward(q, k, v, [lq], [lk], 0.5, c["pre"], c["next"],
+                                        sparse_mode=c["mode"], atten_mask=mask)
+        allowed = np.array(c["allowed"], float)
+        cnt = allowed.sum(axis=1, keepdims=True)
+        want = np.divide(allowed, cnt, out=np.zeros_like(allowed), where=cnt > 0)
+        np.testing.assert_allclose(y[:, 0, :lk], want, rtol=0, atol=1e-15)
+        assert np.all(np.isinf(m[cnt[:, 0] == 0]))
+
+
+def test_causal_mask_tensor_equals_the_causal_mode():
+    """Mode 1 with the lower-triangular mask tensor (masked iff j > i) is the
+    top-left causal mode 2; mode 0 with an all-zero mask is mode 0 alone."""
+    rng = np.random.default_rng(16)
+    lens = [23, 40]
+    T = sum(lens)
+    q, k, v, dy = (rng.standard_normal((T, 2, 8)) for _ in range(4))
+    tri = (np.arange(48)[None, :] > np.arange(48)[:, None]).astype(np.uint8)
+    a = oracle.varlen_forward(q, k, v, lens, lens, 0.3, 0, 0, sparse_mode=1, atten_mask=tri)
+    b = oracle.varlen_forward(q, k, v, lens, lens, 0.3, 0, 0, sparse_mode=2)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+    ga = oracle.varlen_backward(q, k, v, dy, *a, lens, lens, 0.3, 0, 0, sparse_mode=1,
+                                atten_mask=tri)
+    gb = oracle.varlen_backward(q, k, v, dy, *b, lens, lens, 0.3, 0, 0, sparse_mode=2)
+    for x, y in zip(ga, gb):
+        np.testing.assert_array_equal(x, y)
+    zero = np.zeros((48, 48), np.uint8)
+    c = oracle.varlen_forward(q, k, v, lens, lens, 0.3, 6, 3, atten_mask=zero)
+    d = oracle.varlen_forward(q, k, v, lens, lens, 0.3, 6, 3)
+    for x, y in zip(c, d):
+        np.testing.assert_array_equal(x, y)
+
+
+def test_atten_mask_gradients_by_finite_differences():
+    """dQ, dK, dV under a random mask (mode 1) against central differences
+    of L = sum(Y * dY)."""
+    rng = np.random.default_rng(17)
+    lq, lk, d = 5, 6, 3
+    q, dy = rng.standard_normal((lq, 1, d)), rng.standard_normal((lq, 1, d))
+    k, v = rng.standard_normal((lk, 1, d)), rng.standard_normal((lk, 1, d))
+    mask = (rng.random((lq, lk)) < 0.35).astype(np.uint8)
+    sc = 0.7
+
+    def loss(qq, kk, vv):
+        y, _, _ = oracle.varlen_forward(qq, kk, vv, [lq], [lk], sc, 0, 0, sparse_mode=1,
+                                        atten_mask=mask)
+        return float((y * dy).sum())
+
+    y, m, l = oracle.varlen_forward(q, k, v, [lq], [lk], sc, 0, 0, sparse_mode=1,
+                                    atten_mask=mask)
+    g = oracle.varlen_backward(q, k, v, dy, y, m, l, [lq], [lk], sc, 0, 0, sparse_mode=1,
+                               atten_mask=mask)
+    h = 1e-6
+    for which, x in enumerate((q, k, v)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            args = [q.copy(), k.copy(), v.copy()]
+            args[which][idx] += h
+            up = loss(*args)
+            args[which][idx] -= 2 * h
+            num[idx] = (up - loss(*args)) / (2 * h)
+        np.testing.assert_allclose(g[which], num, rtol=1e-6, atol=1e-8)
