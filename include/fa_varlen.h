@@ -34,10 +34,11 @@
  *   the parameter table).  Causal = next_tokens 0, pre_tokens >= max length.
  *   sparse_mode (parameter table row sparseMode; the page defers the
  *   per-mode details to a document it does not include; these are the
- *   readings): 0 and 4 = that window; 2 = lower triangle aligned at the
- *   top-left corner, j <= i; 3 = lower triangle aligned at the bottom-right
- *   corner, j <= i + Lk - Lq.  Modes 2 and 3 ignore pre_tokens / next_tokens
- *   (constraint section).  The outer-split starts of the options structs
+ *   readings): 0 and 4 = that window (and the optional explicit mask of
+ *   the options structs); 1 = the explicit mask alone; 2 = lower triangle
+ *   aligned at the top-left corner, j <= i; 3 = lower triangle aligned at
+ *   the bottom-right corner, j <= i + Lk - Lq.  Modes 1, 2 and 3 ignore
+ *   pre_tokens / next_tokens (constraint section).  The outer-split starts of the options structs
  *   move the chosen window onto global positions.
  *   Grouped heads: query head n uses key/value head n / (head_num/head_num_kv)
  *   (constraint section: Nq/Nkv must be an integer).
@@ -62,7 +63,7 @@
  *                      multiple of head_num_kv, unknown dtype, non-finite
  *                      scale, drop_mask_bytes too small
  *   FA_ERR_UNSUPPORTED a valid request this build does not implement:
- *                      head_dim not in {64, 128}, sparse_mode 1, 6, 7, 8
+ *                      head_dim not in {64, 128}, sparse_mode 6, 7, 8
  *                      (sparse_mode 5 or outside 0..8: FA_ERR_INVALID)
  *   FA_ERR_WORKSPACE   workspace_bytes below the size the size call gave
  *   FA_ERR_CUDA        a CUDA launch or copy failed
@@ -129,12 +130,28 @@ typedef struct {
    * FA_ERR_INVALID.  The forward must be given the same starts. */
   const int64_t *q_start_idx;
   const int64_t *kv_start_idx;
+  /* Explicit attention mask (parameter table row attenMaskOptional; 1 = the
+   * position is excluded, 0 = it takes part): DEVICE uint8 matrix of
+   * atten_mask_rows x atten_mask_cols, row-major, shared by every sequence
+   * and head and indexed by each sequence's chunk-local (i, j).  Read in
+   * sparse_mode 1 (alone) and 0 / 4 (together with the window); modes 2 and
+   * 3 ignore it.  The compute calls with sparse_mode 1 require it
+   * (FA_ERR_NULLPTR otherwise), the size calls do not; a mask with
+   * rows < max Lq or cols < max Lk is FA_ERR_INVALID.  The forward must be
+   * given the same mask. */
+  const uint8_t *atten_mask;
+  int64_t atten_mask_rows;
+  int64_t atten_mask_cols;
 } fa_bwd_options;
 
-/* Options of fa_varlen_fwd_ex. */
+/* Options of fa_varlen_fwd_ex (fields as in fa_bwd_options; NULL / 0 for
+ * none). */
 typedef struct {
-  const int64_t *q_start_idx;   /* as in fa_bwd_options; NULL for 0 */
+  const int64_t *q_start_idx;
   const int64_t *kv_start_idx;
+  const uint8_t *atten_mask;
+  int64_t atten_mask_rows;
+  int64_t atten_mask_cols;
 } fa_fwd_options;
 
 /* Forward workspace size in bytes (same scalar arguments as fa_varlen_fwd). */

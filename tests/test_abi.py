@@ -84,7 +84,7 @@ def test_workspace_size_checks():
     assert _ws(tq=100)[0] == fa.FA_ERR_INVALID
     assert _ws(lens_q=(1 << 20, 1))[0] == fa.FA_ERR_INVALID
     assert _ws(d=96)[0] == fa.FA_ERR_UNSUPPORTED
-    assert _ws(sparse=1)[0] == fa.FA_ERR_UNSUPPORTED
+    assert _ws(sparse=1)[0] == fa.FA_OK
     for mode in (6, 7, 8):
         assert _ws(sparse=mode)[0] == fa.FA_ERR_UNSUPPORTED
     for mode in (-1, 5, 9):
@@ -135,6 +135,7 @@ def test_bwd_argument_checks_before_any_launch():
     assert _bwd_call(n=3, nkv=2) == fa.FA_ERR_INVALID
     assert _bwd_call(d=80) == fa.FA_ERR_UNSUPPORTED
     assert _bwd_call(sparse=6) == fa.FA_ERR_UNSUPPORTED
+    assert _bwd_call(sparse=1) == fa.FA_ERR_NULLPTR           # mode 1 reads the attention mask
     assert _bwd_call(sparse=5) == fa.FA_ERR_INVALID
     assert _bwd_call(ws_bytes=16) == fa.FA_ERR_WORKSPACE
     assert _bwd_call(ws=None, ws_bytes=1 << 20) == fa.FA_ERR_NULLPTR

@@ -112,3 +112,52 @@ def test_sparse_modes_against_oracle(name, impl):
                                            w.keep_prob, sparse_mode=mode)
     assert_close(dict(y=y, dq=dq, dk=dk, dv=dv), dict(y=ry, dq=rdq, dk=rdk, dv=rdv),
                  TOL[w.dtype])
+
+
+def _random_mask(w, seed, density):
+    """Seeded uint8 mask, a few rows / columns wider than the longest sequence."""
+    g = np.random.default_rng(seed)
+    rows, cols = max(w.lens) + 3, max(w.lens_kv) + 5
+    return (g.random((rows, cols)) < density).astype(np.uint8)
+
+
+MASK_CASES = {
+    "mode1_ragged": (wl.Workload(68, "bf16", [100, 260, 0, 37], 2, 128, 0, 0, seed=29,
+                                 lens_kv=[230, 140, 9, 37]), 1, 0.3),
+    "mode0_band_and_mask_gqa": (wl.Workload(69, "bf16", [200, 90], 4, 128, 60, 10, seed=30,
+                                            n_heads_kv=2), 0, 0.2),
+    "mode1_dropout": (wl.Workload(70, "bf16", [150, 64], 2, 128, 0, 0, keep_prob=0.85, seed=31),
+                      1, 0.5),
+    "mode1_fp32": (wl.Workload(71, "fp32", [70, 33], 2, 64, 0, 0, seed=32, lens_kv=[50, 90]),
+                   1, 0.3),
+}
+
+
+@pytest.mark.parametrize("impl", ["simt", "tcgen05"])
+@pytest.mark.parametrize("name", list(MASK_CASES))
+def test_atten_mask_against_oracle(name, impl):
+    w, mode, density = MASK_CASES[name]
+    if impl == "tcgen05" and (w.dtype == "fp32" or w.head_dim != 128):
+        pytest.skip("tcgen05 kernel not built for this case")
+    am_np = _random_mask(w, w.seed, density)
+    am = torch.from_numpy(am_np).to(DEV)
+    tensors = wl.make_tensors(w)
+    mask_np = wl.make_keep_mask(w)
+    mask = None if mask_np is None else torch.from_numpy(mask_np).to(DEV)
+    q, k, v, dy = (t.to(DEV) for t in tensors)
+    y, m, l = fa.fwd(q, k, v, w.lens, w.lens_kv, w.scale, w.pre_tokens, w.next_tokens,
+                     w.keep_prob, mask, sparse_mode=mode, atten_mask=am)
+    dq, dk, dv = fa.bwd(q, k, v, dy, y, m, l, w.lens, w.lens_kv, w.scale, w.pre_tokens,
+                        w.next_tokens, w.keep_prob, mask, impl=IMPLS[impl], sparse_mode=mode,
+                        atten_mask=am)
+    torch.cuda.synchronize()
+    import oracle
+    qn, kn, vn, dyn = (f64(t) for t in tensors)
+    ry, rm, rl = oracle.varlen_forward(qn, kn, vn, w.lens, w.lens_kv, w.scale, w.pre_tokens,
+                                       w.next_tokens, mask_np, w.keep_prob, sparse_mode=mode,
+                                       atten_mask=am_np)
+    rdq, rdk, rdv = oracle.varlen_backward(qn, kn, vn, dyn, ry, rm, rl, w.lens, w.lens_kv,
+                                           w.scale, w.pre_tokens, w.next_tokens, mask_np,
+                                           w.keep_prob, sparse_mode=mode, atten_mask=am_np)
+    assert_close(dict(y=y, dq=dq, dk=dk, dv=dv), dict(y=ry, dq=rdq, dk=rdk, dv=rdv),
+                 TOL[w.dtype])

@@ -33,12 +33,16 @@ class BwdOptions(ctypes.Structure):
     _fields_ = [("impl", ctypes.c_int32), ("deterministic", ctypes.c_int32),
                 ("wait_timeout_ns", ctypes.c_int64), ("events", ctypes.POINTER(ctypes.c_void_p)),
                 ("q_start_idx", ctypes.POINTER(ctypes.c_int64)),
-                ("kv_start_idx", ctypes.POINTER(ctypes.c_int64))]
+                ("kv_start_idx", ctypes.POINTER(ctypes.c_int64)),
+                ("atten_mask", ctypes.c_void_p), ("atten_mask_rows", ctypes.c_int64),
+                ("atten_mask_cols", ctypes.c_int64)]
 
 
 class FwdOptions(ctypes.Structure):
     _fields_ = [("q_start_idx", ctypes.POINTER(ctypes.c_int64)),
-                ("kv_start_idx", ctypes.POINTER(ctypes.c_int64))]
+                ("kv_start_idx", ctypes.POINTER(ctypes.c_int64)),
+                ("atten_mask", ctypes.c_void_p), ("atten_mask_rows", ctypes.c_int64),
+                ("atten_mask_cols", ctypes.c_int64)]
 
 
 class FaError(RuntimeError):
@@ -137,17 +141,27 @@ def _starts(starts):
     return (ctypes.c_int64 * max(1, len(vals)))(*vals)
 
 
+def _mask_fields(atten_mask):
+    """(pointer, rows, cols) of a 2-D uint8 device mask, or (None, 0, 0)."""
+    if atten_mask is None:
+        return None, 0, 0
+    rows, cols = atten_mask.shape
+    return ctypes.c_void_p(atten_mask.data_ptr()), int(rows), int(cols)
+
+
 def _opts(impl=FA_BWD_AUTO, wait_timeout_ns=0, events=None, deterministic=False,
-          q_start=None, kv_start=None):
+          q_start=None, kv_start=None, atten_mask=None):
     ev = None
     if events is not None:
         arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
         ev = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
         ev._keep = arr
     qs, ks = _starts(q_start), _starts(kv_start)
+    am, am_rows, am_cols = _mask_fields(atten_mask)
     opt = BwdOptions(int(impl), int(bool(deterministic)), int(wait_timeout_ns), ev,
                      ctypes.cast(qs, ctypes.POINTER(ctypes.c_int64)) if qs is not None else None,
-                     ctypes.cast(ks, ctypes.POINTER(ctypes.c_int64)) if ks is not None else None)
+                     ctypes.cast(ks, ctypes.POINTER(ctypes.c_int64)) if ks is not None else None,
+                     am, am_rows, am_cols)
     opt._keep = (qs, ks)
     return opt
 
@@ -166,11 +180,11 @@ def fwd_workspace_size(lens_q, lens_kv, n, n_kv, d, dtype, keep_prob=1.0,
 
 def bwd_workspace_size(lens_q, lens_kv, n, n_kv, d, dtype, keep_prob=1.0,
                        pre_tokens=2 ** 31 - 1, next_tokens=2 ** 31 - 1,
-                       impl=FA_BWD_AUTO, sparse_mode=0) -> int:
+                       impl=FA_BWD_AUTO, sparse_mode=0, atten_mask=None) -> int:
     lq, b, tq = _lens(lens_q)
     lk, _, tk = _lens(lens_kv)
     out = ctypes.c_size_t(0)
-    opt = _opts(impl)
+    opt = _opts(impl, atten_mask=atten_mask)
     _check(lib().fa_varlen_bwd_workspace_size_ex(lq, lk, b, tq, tk, n, n_kv, d, _DTYPE[dtype],
                                                  b"TND", keep_prob, pre_tokens, next_tokens,
                                                  int(sparse_mode), ctypes.byref(opt),
@@ -181,11 +195,13 @@ def bwd_workspace_size(lens_q, lens_kv, n, n_kv, d, dtype, keep_prob=1.0,
 
 def fwd(q, k, v, lens_q, lens_kv, scale, pre_tokens, next_tokens, keep_prob=1.0,
         drop_mask=None, y=None, softmax_max=None, softmax_sum=None, workspace=None,
-        stream=None, q_start=None, kv_start=None, sparse_mode=0):
+        stream=None, q_start=None, kv_start=None, sparse_mode=0, atten_mask=None):
     """Y and the [T, N, 8] statistics (fa_varlen_fwd_ex).  ``q_start`` /
     ``kv_start``: per-sequence global chunk starts (outer split), or None.
-    ``sparse_mode``: 0 or 4 (preTokens / nextTokens band), 2 (lower triangle
-    from the top-left corner), 3 (lower triangle from the bottom-right)."""
+    ``sparse_mode``: 0 or 4 (preTokens / nextTokens band), 1 (``atten_mask``
+    alone), 2 (lower triangle from the top-left corner), 3 (lower triangle
+    from the bottom-right).  ``atten_mask``: 2-D uint8 device tensor, 1 =
+    excluded, at each sequence's chunk-local (i, j); read in modes 0, 1, 4."""
     tq, n, d = q.shape
     n_kv = k.shape[1]
     lq, b, _ = _lens(lens_q)
@@ -203,8 +219,10 @@ def fwd(q, k, v, lens_q, lens_kv, scale, pre_tokens, next_tokens, keep_prob=1.0,
         workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
     mask_bytes = 0 if drop_mask is None else drop_mask.numel()
     qs, ks = _starts(q_start), _starts(kv_start)
+    am, am_rows, am_cols = _mask_fields(atten_mask)
     opt = FwdOptions(ctypes.cast(qs, ctypes.POINTER(ctypes.c_int64)) if qs is not None else None,
-                     ctypes.cast(ks, ctypes.POINTER(ctypes.c_int64)) if ks is not None else None)
+                     ctypes.cast(ks, ctypes.POINTER(ctypes.c_int64)) if ks is not None else None,
+                     am, am_rows, am_cols)
     _check(lib().fa_varlen_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(drop_mask), mask_bytes, lq, lk,
                                   b, tq, k.shape[0], n, n_kv, d, _DTYPE[q.dtype], b"TND",
                                   float(scale), float(keep_prob), int(pre_tokens),
@@ -217,7 +235,7 @@ def fwd(q, k, v, lens_q, lens_kv, scale, pre_tokens, next_tokens, keep_prob=1.0,
 def bwd(q, k, v, dy, y, softmax_max, softmax_sum, lens_q, lens_kv, scale, pre_tokens,
         next_tokens, keep_prob=1.0, drop_mask=None, dq=None, dk=None, dv=None,
         workspace=None, stream=None, impl=FA_BWD_AUTO, wait_timeout_ns=0, events=None,
-        deterministic=False, q_start=None, kv_start=None, sparse_mode=0):
+        deterministic=False, q_start=None, kv_start=None, sparse_mode=0, atten_mask=None):
     """dQ, dK, dV (fa_varlen_bwd_ex).  ``events``: four torch.cuda.Event
     (already recorded once, so that they exist) recorded around the kernels.
     ``deterministic``: add the dQ partials in a fixed order (bitwise
@@ -235,10 +253,10 @@ def bwd(q, k, v, dy, y, softmax_max, softmax_sum, lens_q, lens_kv, scale, pre_to
         dv = torch.empty_like(v)
     if workspace is None:
         ws = bwd_workspace_size(lens_q, lens_kv, n, n_kv, d, q.dtype, keep_prob, pre_tokens,
-                                next_tokens, impl, sparse_mode)
+                                next_tokens, impl, sparse_mode, atten_mask)
         workspace = torch.empty(ws, dtype=torch.uint8, device=q.device)
     mask_bytes = 0 if drop_mask is None else drop_mask.numel()
-    opt = _opts(impl, wait_timeout_ns, events, deterministic, q_start, kv_start)
+    opt = _opts(impl, wait_timeout_ns, events, deterministic, q_start, kv_start, atten_mask)
     _check(lib().fa_varlen_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(dy), _ptr(drop_mask),
                                   mask_bytes, _ptr(softmax_max), _ptr(softmax_sum), _ptr(y), lq,
                                   lk, b, tq, k.shape[0], n, n_kv, d, _DTYPE[q.dtype], b"TND",

@@ -43,6 +43,9 @@ struct Problem {
   // Outer split: per-sequence global start of the query / key-value chunk
   // (host arrays of length batch), or null for 0.
   const int64_t *q_start = nullptr, *kv_start = nullptr;
+  // Explicit attention mask (device, rows x cols), or null.
+  const uint8_t *atten_mask = nullptr;
+  int64_t am_rows = 0, am_cols = 0;
 
   // Window of sequence b on chunk-local indices (see SeqInfo::pre).  The
   // sparse mode picks the window on global positions (modes 0 and 4: the
@@ -54,12 +57,17 @@ struct Problem {
     return (q_start ? q_start[b] : 0) - (kv_start ? kv_start[b] : 0);
   }
   int64_t mode_pre(int64_t) const {
-    return (sparse_mode == 2 || sparse_mode == 3) ? (int64_t(1) << 28) : clamp_window(pre);
+    return (sparse_mode >= 1 && sparse_mode <= 3) ? (int64_t(1) << 28) : clamp_window(pre);
   }
   int64_t mode_next(int64_t b) const {
+    if (sparse_mode == 1) return int64_t(1) << 28;
     if (sparse_mode == 2) return 0;
     if (sparse_mode == 3) return lens_kv[b] - lens_q[b];
     return clamp_window(next);
+  }
+  // The mask the kernels read: modes 0, 1 and 4 only.
+  const uint8_t *mask_used() const {
+    return (sparse_mode == 0 || sparse_mode == 1 || sparse_mode == 4) ? atten_mask : nullptr;
   }
   int64_t pre_of(int64_t b) const { return clamp_window(mode_pre(b) - shift(b)); }
   int64_t next_of(int64_t b) const { return clamp_window(mode_next(b) + shift(b)); }
@@ -98,7 +106,15 @@ fa_status check_problem(Problem &pr, const char *layout,
   // sparseMode: 0..8, 5 not supported (parameter table); this build
   // implements the window modes 0, 2, 3 and 4.
   if (pr.sparse_mode < 0 || pr.sparse_mode > 8 || pr.sparse_mode == 5) return FA_ERR_INVALID;
-  if (pr.sparse_mode == 1 || pr.sparse_mode > 4) return FA_ERR_UNSUPPORTED;
+  if (pr.sparse_mode > 4) return FA_ERR_UNSUPPORTED;
+  if (pr.atten_mask != nullptr) {
+    int64_t mq = 0, mk = 0;
+    for (int64_t b = 0; b < pr.batch; ++b) {
+      mq = std::max(mq, pr.lens_q[b]);
+      mk = std::max(mk, pr.lens_kv[b]);
+    }
+    if (pr.am_rows < mq || pr.am_cols < mk || pr.am_cols < 1) return FA_ERR_INVALID;
+  }
   if (pr.d != 64 && pr.d != 128) return FA_ERR_UNSUPPORTED;
   pr.tp = tp;
   pr.mask_bits = bits;
@@ -371,6 +387,9 @@ fa_status fa_varlen_fwd_ex(const void *q, const void *k, const void *v,
   if (options) {
     pr.q_start = options->q_start_idx;
     pr.kv_start = options->kv_start_idx;
+    pr.atten_mask = options->atten_mask;
+    pr.am_rows = options->atten_mask_rows;
+    pr.am_cols = options->atten_mask_cols;
   }
   // Pointers of an empty side (no query rows / no key rows) may be null.
   const bool hq = total_q > 0, hk = total_kv > 0;
@@ -380,6 +399,7 @@ fa_status fa_varlen_fwd_ex(const void *q, const void *k, const void *v,
                                {req(hq, q), req(hk, k), req(hk, v), req(hq, y),
                                 req(hq, softmax_max), req(hq, softmax_sum)});
   if (st != FA_OK) return st;
+  if (pr.sparse_mode == 1 && pr.atten_mask == nullptr) return FA_ERR_NULLPTR;
   const bool dropout = keep_prob < 1.0;
   if (dropout && drop_mask == nullptr) return FA_ERR_NULLPTR;
   if (!std::isfinite(scale)) return FA_ERR_INVALID;
@@ -407,6 +427,8 @@ fa_status fa_varlen_fwd_ex(const void *q, const void *k, const void *v,
   p.scale = float(scale);
   p.inv_keep = float(1.0 / keep_prob);
   p.use_dropout = dropout;
+  p.atten_mask = pr.mask_used();
+  p.am_cols = pr.am_cols;
   if (launch_fwd_simt(p, dtype, cs) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }
@@ -439,6 +461,9 @@ fa_status fa_varlen_bwd_workspace_size_ex(const int64_t *seq_lens_q, const int64
   if (options) {
     pr.q_start = options->q_start_idx;
     pr.kv_start = options->kv_start_idx;
+    pr.atten_mask = options->atten_mask;
+    pr.am_rows = options->atten_mask_rows;
+    pr.am_cols = options->atten_mask_cols;
   }
   fa_status st = check_problem(pr, layout, {});
   if (st != FA_OK) return st;
@@ -479,6 +504,9 @@ fa_status fa_varlen_bwd_ex(const void *q, const void *k, const void *v, const vo
   if (options) {
     pr.q_start = options->q_start_idx;
     pr.kv_start = options->kv_start_idx;
+    pr.atten_mask = options->atten_mask;
+    pr.am_rows = options->atten_mask_rows;
+    pr.am_cols = options->atten_mask_cols;
   }
   // Pointers of an empty side (no query rows / no key rows) may be null.
   const bool hq = total_q > 0, hk = total_kv > 0;
@@ -489,6 +517,7 @@ fa_status fa_varlen_bwd_ex(const void *q, const void *k, const void *v, const vo
       {req(hq, q), req(hk, k), req(hk, v), req(hq, dy), req(hq, softmax_max),
        req(hq, softmax_sum), req(hq, y), req(hq, dq), req(hk, dk), req(hk, dv)});
   if (st != FA_OK) return st;
+  if (pr.sparse_mode == 1 && pr.atten_mask == nullptr) return FA_ERR_NULLPTR;
   const bool dropout = keep_prob < 1.0;
   if (dropout && drop_mask == nullptr) return FA_ERR_NULLPTR;
   if (!std::isfinite(scale)) return FA_ERR_INVALID;
@@ -552,6 +581,8 @@ fa_status fa_varlen_bwd_ex(const void *q, const void *k, const void *v, const vo
   p.use_dropout = dropout;
   p.timeout_ns = (options && options->wait_timeout_ns > 0) ? options->wait_timeout_ns
                                                            : kDefaultTimeoutNs;
+  p.atten_mask = pr.mask_used();
+  p.am_cols = pr.am_cols;
 
   void *const *ev = options ? options->events : nullptr;
   auto mark = [&](int i) {

@@ -35,6 +35,12 @@ __device__ __forceinline__ bool window_ok(int i, int j, int lq, int lk, int pre,
   return i < lq && j < lk && j >= i - pre && j <= i + next;
 }
 
+// Explicit attention mask: true when (i, j) is excluded (mask byte != 0).
+// Callers pass in-range (i, j).
+__device__ __forceinline__ bool atten_masked(const uint8_t *mask, int64_t cols, int i, int j) {
+  return mask != nullptr && __ldg(mask + int64_t(i) * cols + j) != 0;
+}
+
 // Sequence owning padded statistics row `row` (the last sequence whose qpad
 // is <= row; zero-length sequences own no rows).
 __device__ __forceinline__ int seq_of_padded_row(const SeqInfo *seqs, int batch, int row) {

@@ -81,6 +81,10 @@ struct BwdParams {
   float scale, scale_log2, inv_keep;
   int use_dropout;
   long long timeout_ns;
+  // Explicit attention mask (uint8 [rows][am_cols], 1 = excluded) at each
+  // sequence's chunk-local (i, j), or null.
+  const uint8_t *atten_mask;
+  int64_t am_cols;
 };
 
 struct FwdParams {
@@ -94,6 +98,8 @@ struct FwdParams {
   int n_items, batch, n, n_kv, d;
   float scale, inv_keep;
   int use_dropout;
+  const uint8_t *atten_mask;   // as BwdParams::atten_mask
+  int64_t am_cols;
 };
 
 // Kernel launchers (return the launch error).

@@ -284,7 +284,8 @@ __global__ void __launch_bounds__(256) bwd_simt_kernel(BwdParams p) {
           const int j = tx + 16 * b;
           const int gi = q0 + i, gj = k0 + j;
           float pv = 0.f, zs = 1.f;
-          if (window_ok(gi, gj, s.len_q, s.len_k, s.pre, s.next)) {
+          if (window_ok(gi, gj, s.len_q, s.len_k, s.pre, s.next) &&
+              !atten_masked(p.atten_mask, p.am_cols, gi, gj)) {
             pv = exp2f(sa[a][b] * p.scale_log2 - lse_s[i]);
             if (p.use_dropout)
               zs = keep_bit(p.mask, s.mask_off, n, s.len_q, s.len_k, gi, gj) * p.inv_keep;
@@ -464,8 +465,9 @@ __global__ void __launch_bounds__(256) fwd_simt_kernel(FwdParams p) {
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
         const int gj = k0 + tx + 16 * b;
-        sv[b] = window_ok(gi, gj, s.len_q, s.len_k, s.pre, s.next) ? sa[a][b] * p.scale
-                                                                   : -CUDART_INF_F;
+        const bool ok = window_ok(gi, gj, s.len_q, s.len_k, s.pre, s.next) &&
+                        !atten_masked(p.atten_mask, p.am_cols, gi, gj);
+        sv[b] = ok ? sa[a][b] * p.scale : -CUDART_INF_F;
         mx = fmaxf(mx, sv[b]);
       }
 #pragma unroll
