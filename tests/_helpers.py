@@ -91,14 +91,16 @@ def assert_close(got: dict, ref: dict, tol: float, keys=("y", "dq", "dk", "dv"))
 def unit_check(w: wl.Workload, tensors, out: dict, b: int, n: int):
     """Oracle forward + backward of one whole (sequence, head) unit of a
     full-size run, compared element by element with the GPU outputs of that
-    unit (max|ref| taken over the unit).  Returns the relative errors."""
+    unit (max|ref| taken over the unit).  The inputs may live on the host or
+    the device; only the unit's slices are copied.  Returns the relative
+    errors."""
     cq, ck = oracle.cu_seqlens(w.lens), oracle.cu_seqlens(w.lens_kv)
     group = w.n_heads // w.n_heads_kv
     q, k, v, dy = tensors
-    qs = q[cq[b]:cq[b + 1], n].double().numpy()
-    ks = k[ck[b]:ck[b + 1], n // group].double().numpy()
-    vs = v[ck[b]:ck[b + 1], n // group].double().numpy()
-    dys = dy[cq[b]:cq[b + 1], n].double().numpy()
+    qs = f64(q[cq[b]:cq[b + 1], n])
+    ks = f64(k[ck[b]:ck[b + 1], n // group])
+    vs = f64(v[ck[b]:ck[b + 1], n // group])
+    dys = f64(dy[cq[b]:cq[b + 1], n])
     keep_rows, _ = cpu_keep_rows(w, b, n)
     y, m, l = oracle.unit_forward(qs, ks, vs, w.scale, w.pre_tokens, w.next_tokens,
                                   keep_rows, w.keep_prob)

@@ -308,8 +308,14 @@ size_t fwd_layout_total(const Problem &pr, size_t *seqs_off, size_t *items_off) 
   return off;
 }
 
-// Uploads [header | seqs | items | table] with one copy; the header's error
-// word and ticket are 0.
+// Copies from pageable memory of at most this size return without waiting
+// for the stream; larger ones can make the host wait until the stream has
+// drained, which would leave the GPU idle while the host builds the next
+// call.  Larger plans therefore go up in pieces of this size.
+constexpr size_t kPageableCopyPiece = size_t(64) << 10;
+
+// Uploads [header | seqs | items | table]; the header's error word and
+// ticket are 0.
 fa_status upload_plan(void *ws, size_t seqs_off, size_t items_off,
                       const std::vector<SeqInfo> &seqs, const std::vector<WorkItem> &items,
                       cudaStream_t st, size_t table_off = 0,
@@ -322,8 +328,12 @@ fa_status upload_plan(void *ws, size_t seqs_off, size_t items_off,
     std::memcpy(host.data() + items_off, items.data(), sizeof(WorkItem) * items.size());
   if (table && !table->empty())
     std::memcpy(host.data() + table_off, table->data(), sizeof(int32_t) * table->size());
-  if (cudaMemcpyAsync(ws, host.data(), bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
-    return FA_ERR_CUDA;
+  for (size_t off = 0; off < bytes; off += kPageableCopyPiece) {
+    const size_t n = std::min(kPageableCopyPiece, bytes - off);
+    if (cudaMemcpyAsync(static_cast<uint8_t *>(ws) + off, host.data() + off, n,
+                        cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return FA_ERR_CUDA;
+  }
   return FA_OK;
 }
 

@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (p.atten_mask != nullptr && jg < sq.len_k) {
         // Explicit mask: for each of its 32 queries a warp reads 32
         // consecutive bytes (its 32 keys) of one mask row.
-#pragma unroll 4
+#pragma unroll
         for (int c = 0; c < 32; ++c) {
           const int i = i0 + c;
           if (i < sq.len_q && atten_masked(p.atten_mask, p.am_cols, i, jg)) pr[c] = 0.f;

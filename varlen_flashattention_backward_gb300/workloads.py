@@ -147,6 +147,26 @@ def make_tensors(w: Workload):
     return q.to(dt), k.to(dt), v.to(dt), dy.to(dt)
 
 
+def make_tensors_on_device(w: Workload, device):
+    """Q, K, V, dY drawn on ``device`` by torch's seeded generator there.
+
+    For inputs of billions of values, where drawing them on the host would
+    take minutes; the values differ from ``make_tensors`` but are fixed by
+    the seed.  Callers hand slices of them to the oracle."""
+    g = torch.Generator(device=device).manual_seed(w.seed)
+    shp_q = (w.total_q, w.n_heads, w.head_dim)
+    shp_k = (w.total_kv, w.n_heads_kv, w.head_dim)
+    dt = w.torch_dtype
+    out = []
+    for shp, std in ((shp_q, 1.0), (shp_k, 1.0), (shp_k, 1.0), (shp_q, w.dy_std)):
+        t = torch.randn(shp, generator=g, dtype=torch.float32, device=device)
+        if std != 1.0:
+            t.mul_(std)
+        out.append(t.to(dt))
+        del t
+    return tuple(out)
+
+
 # ---------------------------------------------------------------------------
 # SplitMix64 dropout keep bits (CPU side of the generator pair)
 # ---------------------------------------------------------------------------
