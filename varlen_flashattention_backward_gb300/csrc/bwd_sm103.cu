@@ -186,9 +186,11 @@ __device__ __forceinline__ bool wait_or_abort(const Ctl &c, uint32_t bar, uint32
   return false;
 }
 
-// kDet: the deterministic mode (ticket-ordered items, ordered dQ adds); a
-// separate instantiation so that the default kernel carries none of it.
-template <bool kBF16, bool kDet>
+// kDet: the deterministic mode (ticket-ordered items, ordered dQ adds).
+// kMask: an explicit attention mask is read.  Each is a separate
+// instantiation so that the default kernel carries none of its code (the
+// mask's untaken branch alone cost 5-10% of the default kernel's time).
+template <bool kBF16, bool kDet, bool kMask>
 __global__ void __launch_bounds__(NTHREADS, 1)
     bwd_tc_kernel(const BwdParams p, const __grid_constant__ TcMaps maps) {
   extern __shared__ uint8_t smem_raw[];
@@ -438,7 +440,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (!(jg <= i + sq.next && jg >= i - sq.pre && jg < sq.len_k)) pr[c] = 0.f;
         }
       }
-      if (p.atten_mask != nullptr && jg < sq.len_k) {
+      if (kMask && jg < sq.len_k) {
         // Explicit mask: for each of its 32 queries a warp reads 32
         // consecutive bytes (its 32 keys) of one mask row.
 #pragma unroll
@@ -739,7 +741,7 @@ bool make_map(CUtensorMap *m, const void *base, int64_t rows, int heads, int box
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kBF16, bool kDet>
+template <bool kBF16, bool kDet, bool kMask>
 cudaError_t launch_t(const BwdParams &p, cudaStream_t st) {
   TcMaps maps;
   if (!make_map(&maps.q, p.q, p.total_q, p.n, BM, kBF16) ||
@@ -749,7 +751,7 @@ cudaError_t launch_t(const BwdParams &p, cudaStream_t st) {
       !make_map(&maps.dk, p.dk, p.total_kv, p.n_kv, BN, kBF16) ||
       !make_map(&maps.dv, p.dv, p.total_kv, p.n_kv, BN, kBF16))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<kBF16, kDet>,
+  cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<kBF16, kDet, kMask>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   int dev = 0;
@@ -758,8 +760,16 @@ cudaError_t launch_t(const BwdParams &p, cudaStream_t st) {
   if ((e = cudaDeviceGetAttribute(&q.prefetch_ahead, cudaDevAttrMultiProcessorCount, dev)) !=
       cudaSuccess)
     return e;
-  bwd_tc_kernel<kBF16, kDet><<<p.n_items, NTHREADS, SMEM_BYTES, st>>>(q, maps);
+  bwd_tc_kernel<kBF16, kDet, kMask><<<p.n_items, NTHREADS, SMEM_BYTES, st>>>(q, maps);
   return cudaGetLastError();
+}
+
+template <bool kBF16>
+cudaError_t launch_dt(const BwdParams &p, cudaStream_t s) {
+  const bool mask = p.atten_mask != nullptr;
+  if (p.deterministic)
+    return mask ? launch_t<kBF16, true, true>(p, s) : launch_t<kBF16, true, false>(p, s);
+  return mask ? launch_t<kBF16, false, true>(p, s) : launch_t<kBF16, false, false>(p, s);
 }
 
 }  // namespace
@@ -776,10 +786,8 @@ bool tcgen05_supported(fa_dtype dt, int head_dim) {
 }
 
 cudaError_t launch_bwd_tcgen05(const BwdParams &p, fa_dtype dt, cudaStream_t s) {
-  if (dt == FA_DTYPE_BF16)
-    return p.deterministic ? launch_t<true, true>(p, s) : launch_t<true, false>(p, s);
-  if (dt == FA_DTYPE_FP16)
-    return p.deterministic ? launch_t<false, true>(p, s) : launch_t<false, false>(p, s);
+  if (dt == FA_DTYPE_BF16) return launch_dt<true>(p, s);
+  if (dt == FA_DTYPE_FP16) return launch_dt<false>(p, s);
   return cudaErrorInvalidValue;
 }
 
