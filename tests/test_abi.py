@@ -83,7 +83,10 @@ def test_workspace_size_checks():
     assert _ws(lens_q=(5, -1))[0] == fa.FA_ERR_INVALID
     assert _ws(tq=100)[0] == fa.FA_ERR_INVALID
     assert _ws(lens_q=(1 << 20, 1))[0] == fa.FA_ERR_INVALID
-    assert _ws(d=96)[0] == fa.FA_ERR_UNSUPPORTED
+    for d in (16, 80, 256, 768):
+        assert _ws(d=d)[0] == fa.FA_ERR_UNSUPPORTED
+    for d in (32, 64, 96, 128, 192):
+        assert _ws(d=d)[0] == fa.FA_OK
     assert _ws(sparse=1)[0] == fa.FA_OK
     for mode in (6, 7, 8):
         assert _ws(sparse=mode)[0] == fa.FA_ERR_UNSUPPORTED

@@ -55,6 +55,12 @@ SMALL = {
     "gqa_band_dropout": wl.Workload(11, "bf16", [300, 0, 150], 4, 128, 100, 20, keep_prob=0.8,
                                     seed=4, n_heads_kv=2),
     "d64_nomask": wl.Workload(12, "bf16", [130, 70], 2, 64, BIG, BIG, seed=5),
+    "d32_band": wl.Workload(16, "bf16", [90, 0, 141], 2, 32, 25, 7, seed=9),
+    "d96_causal_gqa_fp16": wl.Workload(17, "fp16", [77, 130], 4, 96, BIG, 0, seed=10,
+                                       n_heads_kv=2),
+    "d192_dropout": wl.Workload(18, "bf16", [66, 129], 2, 192, BIG, BIG, keep_prob=0.85,
+                                seed=11),
+    "d96_fp32": wl.Workload(19, "fp32", [40, 71], 2, 96, 30, 30, seed=12),
     "fp16_causal": wl.Workload(13, "fp16", [100, 33], 2, 128, BIG, 0, seed=6),
     "lq_ne_lk": wl.Workload(14, "bf16", [50, 90], 2, 128, 30, 10, seed=7, lens_kv=[120, 40]),
     "fp32_dropout_band": wl.Workload(15, "fp32", [70, 45], 2, 128, 20, 3, keep_prob=0.7, seed=8),

@@ -559,7 +559,8 @@ __global__ void gen_keep_mask_kernel(uint8_t *mask, int64_t nbits, uint64_t seed
 
 template <typename T, int D>
 cudaError_t launch_bwd_simt_t(const BwdParams &p, cudaStream_t st) {
-  const int smem = (4 * 64 * (D + 1) + 2 * 64 * (kQTile + 1) + 128) * int(sizeof(float));
+  constexpr int smem = (4 * 64 * (D + 1) + 2 * 64 * (kQTile + 1) + 128) * int(sizeof(float));
+  static_assert(D % 16 == 0 && smem <= 227 * 1024, "CUDA-core backward tiles");
   cudaError_t e = cudaFuncSetAttribute(bwd_simt_kernel<T, D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -580,10 +581,17 @@ cudaError_t launch_fwd_simt_t(const FwdParams &p, cudaStream_t st) {
 template <typename T, int D>
 cudaError_t launch_pre_t(const BwdParams &p, cudaStream_t st) {
   dim3 grid(p.tp / kQTile, p.n);
-  if (((reinterpret_cast<uintptr_t>(p.dy) | reinterpret_cast<uintptr_t>(p.y)) & 15u) == 0)
-    preprocess_vec_kernel<T, D><<<grid, 256, 0, st>>>(p);
-  else
-    preprocess_kernel<T, D><<<grid, 256, 0, st>>>(p);
+  // The 16-byte-load kernel packs whole rows into a warp: it needs the lanes
+  // of one row to divide 32.
+  constexpr int kLanes = D / (16 / int(sizeof(T)));
+  constexpr bool kVecShape = kLanes <= 32 && 32 % kLanes == 0 && (kQTile / 8) % (32 / kLanes) == 0;
+  if constexpr (kVecShape) {
+    if (((reinterpret_cast<uintptr_t>(p.dy) | reinterpret_cast<uintptr_t>(p.y)) & 15u) == 0) {
+      preprocess_vec_kernel<T, D><<<grid, 256, 0, st>>>(p);
+      return cudaGetLastError();
+    }
+  }
+  preprocess_kernel<T, D><<<grid, 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 
@@ -606,17 +614,21 @@ cudaError_t launch_conv_t(const BwdParams &p, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// Head dims built for the CUDA-core kernels (multiples of 16, up to the
+// largest whose backward tiles fit in 227 KB of shared memory).
+#define FAV_DISPATCH_D(dt, d, DV, FN, ...)                                                \
+  if ((d) == DV) {                                                                        \
+    if ((dt) == FA_DTYPE_FP32) return FN<float, DV>(__VA_ARGS__);                         \
+    if ((dt) == FA_DTYPE_BF16) return FN<__nv_bfloat16, DV>(__VA_ARGS__);                 \
+    if ((dt) == FA_DTYPE_FP16) return FN<__half, DV>(__VA_ARGS__);                        \
+  }
 #define FAV_DISPATCH(dt, d, FN, ...)                                                      \
   do {                                                                                    \
-    if ((d) == 64) {                                                                      \
-      if ((dt) == FA_DTYPE_FP32) return FN<float, 64>(__VA_ARGS__);                       \
-      if ((dt) == FA_DTYPE_BF16) return FN<__nv_bfloat16, 64>(__VA_ARGS__);               \
-      if ((dt) == FA_DTYPE_FP16) return FN<__half, 64>(__VA_ARGS__);                      \
-    } else if ((d) == 128) {                                                              \
-      if ((dt) == FA_DTYPE_FP32) return FN<float, 128>(__VA_ARGS__);                      \
-      if ((dt) == FA_DTYPE_BF16) return FN<__nv_bfloat16, 128>(__VA_ARGS__);              \
-      if ((dt) == FA_DTYPE_FP16) return FN<__half, 128>(__VA_ARGS__);                     \
-    }                                                                                     \
+    FAV_DISPATCH_D(dt, d, 32, FN, __VA_ARGS__)                                            \
+    FAV_DISPATCH_D(dt, d, 64, FN, __VA_ARGS__)                                            \
+    FAV_DISPATCH_D(dt, d, 96, FN, __VA_ARGS__)                                            \
+    FAV_DISPATCH_D(dt, d, 128, FN, __VA_ARGS__)                                           \
+    FAV_DISPATCH_D(dt, d, 192, FN, __VA_ARGS__)                                           \
     return cudaErrorInvalidValue;                                                         \
   } while (0)
 
