@@ -438,7 +438,9 @@ def run_cuda(args, w):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_src} bf16_tflops (burst)",
+                     "frac_of_sustained": achieved / float(peaks["bf16_tflops_sustained"]),
                      "kernel": kernel_tag, "kernel_ms": main_avg},
+        "ms_per_step_median": statistics.median(step_ms),
         "kernel_ms": {"preprocess": sum(pre_ms) / len(pre_ms), "main": main_avg,
                       "dq_convert": sum(conv_ms) / len(conv_ms)},
         "cpu_baseline": cpu,
@@ -461,7 +463,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6])
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7])
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tcgen05"])
     ap.add_argument("--ref-budget", type=float, default=10.0,
                     help="seconds of oracle work per timed sample")

@@ -64,8 +64,9 @@
  *                      scale, drop_mask_bytes too small
  *   FA_ERR_UNSUPPORTED a valid request this build does not implement:
  *                      head_dim not in {32, 64, 96, 128, 192} (the
- *                      tensor-core backward takes 128; the others run on
- *                      the CUDA-core kernels), sparse_mode 6, 7, 8
+ *                      tensor-core backward takes 64 and 128 in 16-bit
+ *                      types; the rest run on the CUDA-core kernels),
+ *                      sparse_mode 6, 7, 8
  *                      (sparse_mode 5 or outside 0..8: FA_ERR_INVALID)
  *   FA_ERR_WORKSPACE   workspace_bytes below the size the size call gave
  *   FA_ERR_CUDA        a CUDA launch or copy failed

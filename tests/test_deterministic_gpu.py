@@ -25,6 +25,8 @@ CASES = {
                                     seed=14, n_heads_kv=2),
     "lq_ne_lk": wl.Workload(42, "bf16", [50, 300], 2, 128, 30, 10, seed=15, lens_kv=[120, 40]),
     "fp32_band": wl.Workload(43, "fp32", [170, 45], 2, 64, 20, 3, seed=16),
+    "d64_gqa_causal": wl.Workload(44, "bf16", [260, 0, 400], 4, 64, BIG, 0, seed=17,
+                                  n_heads_kv=2),
 }
 
 
@@ -51,7 +53,7 @@ def _run(w, tensors, mask, impl, deterministic, stats=None):
 @pytest.mark.parametrize("name", list(CASES))
 def test_deterministic_is_bitwise_repeatable_and_correct(name, impl):
     w = CASES[name]
-    if impl == "tcgen05" and (w.dtype == "fp32" or w.head_dim != 128):
+    if impl == "tcgen05" and (w.dtype == "fp32" or w.head_dim not in (64, 128)):
         pytest.skip("tcgen05 kernel not built for this case")
     tensors = wl.make_tensors(w)
     mask = device_mask(w, DEV)

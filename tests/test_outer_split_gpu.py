@@ -40,7 +40,7 @@ def built():
 @pytest.mark.parametrize("name", list(CASES))
 def test_starts_against_oracle(name, impl):
     w, qs, ks = CASES[name]
-    if impl == "tcgen05" and (w.dtype == "fp32" or w.head_dim != 128):
+    if impl == "tcgen05" and (w.dtype == "fp32" or w.head_dim not in (64, 128)):
         pytest.skip("tcgen05 kernel not built for this case")
     tensors = wl.make_tensors(w)
     mask_np = wl.make_keep_mask(w)
@@ -92,7 +92,7 @@ MODE_CASES = {
 @pytest.mark.parametrize("name", list(MODE_CASES))
 def test_sparse_modes_against_oracle(name, impl):
     w, mode = MODE_CASES[name]
-    if impl == "tcgen05" and (w.dtype == "fp32" or w.head_dim != 128):
+    if impl == "tcgen05" and (w.dtype == "fp32" or w.head_dim not in (64, 128)):
         pytest.skip("tcgen05 kernel not built for this case")
     tensors = wl.make_tensors(w)
     mask_np = wl.make_keep_mask(w)
@@ -130,6 +130,8 @@ MASK_CASES = {
                       1, 0.5),
     "mode1_fp32": (wl.Workload(71, "fp32", [70, 33], 2, 64, 0, 0, seed=32, lens_kv=[50, 90]),
                    1, 0.3),
+    "mode1_d64": (wl.Workload(72, "bf16", [140, 70], 2, 64, 0, 0, seed=33, lens_kv=[90, 200]),
+                  1, 0.3),
 }
 
 
@@ -137,7 +139,7 @@ MASK_CASES = {
 @pytest.mark.parametrize("name", list(MASK_CASES))
 def test_atten_mask_against_oracle(name, impl):
     w, mode, density = MASK_CASES[name]
-    if impl == "tcgen05" and (w.dtype == "fp32" or w.head_dim != 128):
+    if impl == "tcgen05" and (w.dtype == "fp32" or w.head_dim not in (64, 128)):
         pytest.skip("tcgen05 kernel not built for this case")
     am_np = _random_mask(w, w.seed, density)
     am = torch.from_numpy(am_np).to(DEV)

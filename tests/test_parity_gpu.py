@@ -56,6 +56,11 @@ SMALL = {
                                     seed=4, n_heads_kv=2),
     "d64_nomask": wl.Workload(12, "bf16", [130, 70], 2, 64, BIG, BIG, seed=5),
     "d32_band": wl.Workload(16, "bf16", [90, 0, 141], 2, 32, 25, 7, seed=9),
+    "d64_causal_ragged_fp16": wl.Workload(20, "fp16", [1, 0, 37, 65, 127, 129, 300], 2, 64,
+                                          BIG, 0, seed=13),
+    "d64_gqa_band_dropout": wl.Workload(21, "bf16", [300, 0, 150], 4, 64, 100, 20,
+                                        keep_prob=0.8, seed=14, n_heads_kv=2),
+    "d64_w7": wl.workload(7),
     "d96_causal_gqa_fp16": wl.Workload(17, "fp16", [77, 130], 4, 96, BIG, 0, seed=10,
                                        n_heads_kv=2),
     "d192_dropout": wl.Workload(18, "bf16", [66, 129], 2, 192, BIG, BIG, keep_prob=0.85,

@@ -115,8 +115,8 @@ fa_status check_problem(Problem &pr, const char *layout,
     }
     if (pr.am_rows < mq || pr.am_cols < mk || pr.am_cols < 1) return FA_ERR_INVALID;
   }
-  // Head dims with kernels: the CUDA-core kernels take multiples of 16 from
-  // this list; the tensor-core backward takes 128.
+  // Head dims with kernels: the CUDA-core kernels take every one of this
+  // list; the tensor-core backward takes 64 and 128.
   if (pr.d != 32 && pr.d != 64 && pr.d != 96 && pr.d != 128 && pr.d != 192)
     return FA_ERR_UNSUPPORTED;
   pr.tp = tp;

@@ -190,9 +190,15 @@ __device__ __forceinline__ bool wait_or_abort(const Ctl &c, uint32_t bar, uint32
 // kMask: an explicit attention mask is read.  Each is a separate
 // instantiation so that the default kernel carries none of its code (the
 // mask's untaken branch alone cost 5-10% of the default kernel's time).
-template <bool kBF16, bool kDet, bool kMask>
+// kD64: head dim 64.  Only the first 64-column box of each tile is loaded;
+// S^T and dP^T take 4 k-steps and dV, dK are N = 64 products.  dQ^T keeps
+// M = 128 (d) with the second K box zeroed, so its rows 64-127 are zero
+// and are not reduced.
+template <bool kBF16, bool kDet, bool kMask, bool kD64>
 __global__ void __launch_bounds__(NTHREADS, 1)
     bwd_tc_kernel(const BwdParams p, const __grid_constant__ TcMaps maps) {
+  constexpr int DD = kD64 ? 64 : HD;   // head dim of the tensors
+  constexpr int NBOX = DD / 64;         // 64-column boxes per row
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~uintptr_t(1023));
@@ -239,6 +245,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tmem_alloc(smem_u32(&s_tmem), 512);
     tmem_relinquish();
   }
+  if constexpr (kD64) {
+    // The second K box (d 64-127) feeds the M = 128 dQ^T product: zero it.
+    for (uint32_t o = threadIdx.x * 16u; o < 16384u; o += NTHREADS * 16u)
+      st_shared_v4(sb + SM_K + 16384u + o, 0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -262,21 +274,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_prefetch_map(&maps.v);
       }
       __syncwarp();
-      const int ky = sq.cu_k + k0, kx = kvh * HD;
-      mbar_arrive_expect_tx_w(bar(B_KV), 4 * 16384);
-      tma_load_2d_w(sb + SM_K, &maps.k, bar(B_KV), kx, ky);
-      tma_load_2d_w(sb + SM_K + 16384, &maps.k, bar(B_KV), kx + 64, ky);
-      tma_load_2d_w(sb + SM_V, &maps.v, bar(B_KV), kx, ky);
-      tma_load_2d_w(sb + SM_V + 16384, &maps.v, bar(B_KV), kx + 64, ky);
+      const int ky = sq.cu_k + k0, kx = kvh * DD;
+      mbar_arrive_expect_tx_w(bar(B_KV), 2 * NBOX * 16384);
+      for (int bx = 0; bx < NBOX; ++bx) {
+        tma_load_2d_w(sb + SM_K + bx * 16384, &maps.k, bar(B_KV), kx + 64 * bx, ky);
+        tma_load_2d_w(sb + SM_V + bx * 16384, &maps.v, bar(B_KV), kx + 64 * bx, ky);
+      }
       // The item `prefetch_ahead` places further down the list starts on
       // some SM about when this one ends: bring its K and V into L2 now.
       if (lane == 0 && blockIdx.x + p.prefetch_ahead < p.n_items) {
         const WorkItem nx = p.items[blockIdx.x + p.prefetch_ahead];
-        const int nky = p.seqs[nx.seq].cu_k + nx.tile * BN, nkx = nx.head * HD;
-        tma_prefetch_l2_2d(&maps.k, nkx, nky);
-        tma_prefetch_l2_2d(&maps.k, nkx + 64, nky);
-        tma_prefetch_l2_2d(&maps.v, nkx, nky);
-        tma_prefetch_l2_2d(&maps.v, nkx + 64, nky);
+        const int nky = p.seqs[nx.seq].cu_k + nx.tile * BN, nkx = nx.head * DD;
+        for (int bx = 0; bx < NBOX; ++bx) {
+          tma_prefetch_l2_2d(&maps.k, nkx + 64 * bx, nky);
+          tma_prefetch_l2_2d(&maps.v, nkx + 64 * bx, nky);
+        }
       }
       __syncwarp();
       int issued = 0;
@@ -287,14 +299,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           break;
         const int n = kvh * group + L / qcnt;
         const int q0 = (qlo + L % qcnt) * BM;
-        const int qy = sq.cu_q + q0, qx = n * HD;
+        const int qy = sq.cu_q + q0, qx = n * DD;
         const uint32_t full = bar(B_FULL + st);
         const int64_t srow = int64_t(n) * p.tp + sq.qpad + q0;
-        mbar_arrive_expect_tx_w(full, 4 * 8192 + 2 * 256);
-        tma_load_2d_w(sb + SM_Q + st * 16384, &maps.q, full, qx, qy);
-        tma_load_2d_w(sb + SM_Q + st * 16384 + 8192, &maps.q, full, qx + 64, qy);
-        tma_load_2d_w(sb + SM_DY + st * 16384, &maps.dy, full, qx, qy);
-        tma_load_2d_w(sb + SM_DY + st * 16384 + 8192, &maps.dy, full, qx + 64, qy);
+        mbar_arrive_expect_tx_w(full, 2 * NBOX * 8192 + 2 * 256);
+        for (int bx = 0; bx < NBOX; ++bx) {
+          tma_load_2d_w(sb + SM_Q + st * 16384 + bx * 8192, &maps.q, full, qx + 64 * bx, qy);
+          tma_load_2d_w(sb + SM_DY + st * 16384 + bx * 8192, &maps.dy, full, qx + 64 * bx, qy);
+        }
         bulk_load_w(sb + SM_LSE + st * 256, p.lse2 + srow, 256, full);
         bulk_load_w(sb + SM_DSUM + st * 256, p.dsum + srow, 256, full);
         ++issued;
@@ -317,7 +329,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // one elected lane per MMA (see mma_ss_w).
     if (n_it > 0) {
       const uint32_t id_s = idesc_f16(128, BM, false, false, kBF16);   // S^T, dP^T
-      const uint32_t id_g = idesc_f16(128, HD, false, true, kBF16);    // dV, dK
+      const uint32_t id_g = idesc_f16(128, DD, false, true, kBF16);    // dV, dK
       const uint32_t id_q = idesc_f16(128, BM, true, true, kBF16);     // dQ^T
       // Descriptors are built once per operand; a k-step adds its byte offset
       // >> 4 to the 14-bit start-address field (shared addresses stay below
@@ -338,7 +350,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const uint64_t bq = sdesc_sw128(sb + SM_Q + st * 16384, 16, 1024);
           const uint64_t by = sdesc_sw128(sb + SM_DY + st * 16384, 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk) {
+          for (int kk = 0; kk < DD / 16; ++kk) {
             const uint32_t ao = (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
             const uint32_t bo = (((kk >> 2) * 8192 + (kk & 3) * 32) >> 4);
             const uint32_t acc = kk > 0 ? 1u : 0u;
@@ -538,7 +550,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint32_t col = half == 0 ? COL_DV : COL_DK;
       const uint32_t stage = sb + (half == 0 ? SM_Q : SM_DY);
 #pragma unroll 1
-      for (int c0 = 0; c0 < HD; c0 += 32) {
+      for (int c0 = 0; c0 < DD; c0 += 32) {
         uint32_t r[32];
         if (n_it > 0) {
           tmem_ld32(tmem + lane_off + col + c0, r);
@@ -567,9 +579,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (quarter == 0 && lane == 0 &&
           wait_or_abort(ctl, bar(B_EPI + half), 0, ROLE_EPILOGUE)) {
         const CUtensorMap *m = half == 0 ? &maps.dv : &maps.dk;
-        const int y = sq.cu_k + k0, x = kvh * HD;
-        tma_store_2d(m, stage, x, y);
-        tma_store_2d(m, stage + 16384, x + 64, y);
+        const int y = sq.cu_k + k0, x = kvh * DD;
+        for (int bx = 0; bx < NBOX; ++bx) tma_store_2d(m, stage + bx * 16384, x + 64 * bx, y);
         bulk_commit_group();
         bulk_wait_group_read0();
       }
@@ -579,9 +590,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const float sc = half == 0 ? 1.f : p.scale;
       const uint32_t col = half == 0 ? COL_DV : COL_DK;
       const bool valid = jg < sq.len_k;
-      T *rowp = out + ((int64_t(sq.cu_k) + jg) * p.n_kv + kvh) * HD;
+      T *rowp = out + ((int64_t(sq.cu_k) + jg) * p.n_kv + kvh) * DD;
 #pragma unroll 1
-      for (int c0 = 0; c0 < HD; c0 += 32) {
+      for (int c0 = 0; c0 < DD; c0 += 32) {
         uint32_t r[32];
         if (n_it > 0) {
           tmem_ld32(tmem + lane_off + col + c0, r);
@@ -606,7 +617,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // ------------------------------------------------------------ dQ drain
     const int quarter = warp & 3;
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
-    const int64_t row_stride = int64_t(p.n) * HD;
+    const int64_t row_stride = int64_t(p.n) * DD;
     for (int L = 0; L < n_it; ++L) {
       const int n = kvh * group + L / qcnt;
       const int q0 = (qlo + L % qcnt) * BM;
@@ -664,12 +675,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         out[4 * j + 2] = hi1 ? u1 : r2;
         out[4 * j + 3] = hi1 ? r3 : u1;
       }
-      float *ptr = p.dq_acc + (int64_t(sq.cu_q) + q0 + c) * row_stride + int64_t(n) * HD +
+      float *ptr = p.dq_acc + (int64_t(sq.cu_q) + q0 + c) * row_stride + int64_t(n) * DD +
                    quarter * 32 + (lane & ~3);
+      if (quarter * 32 < DD) {   // lanes d >= DD hold the zero rows of a padded K
 #pragma unroll
-      for (int j = 0; j < BM / 4; ++j, ptr += 4 * row_stride)
-        if (4 * j + c < rows)
-          red_add_v4_f32(ptr, out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
+        for (int j = 0; j < BM / 4; ++j, ptr += 4 * row_stride)
+          if (4 * j + c < rows)
+            red_add_v4_f32(ptr, out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
+      }
       if constexpr (kDet) {
         __threadfence();
         drain_bar_sync();
@@ -727,12 +740,13 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [rows, heads * 128] 16-bit tensor as a 2-D map with 64-column x box_rows boxes.
-bool make_map(CUtensorMap *m, const void *base, int64_t rows, int heads, int box_rows, bool bf16) {
+// [rows, heads * d] 16-bit tensor as a 2-D map with 64-column x box_rows boxes.
+bool make_map(CUtensorMap *m, const void *base, int64_t rows, int heads, int d, int box_rows,
+              bool bf16) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
-  cuuint64_t dims[2] = {cuuint64_t(heads) * HD, cuuint64_t(rows)};
-  cuuint64_t strides[1] = {cuuint64_t(heads) * HD * 2};
+  cuuint64_t dims[2] = {cuuint64_t(heads) * d, cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(heads) * d * 2};
   cuuint32_t box[2] = {64, cuuint32_t(box_rows)};
   cuuint32_t es[2] = {1, 1};
   return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
@@ -741,17 +755,18 @@ bool make_map(CUtensorMap *m, const void *base, int64_t rows, int heads, int box
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kBF16, bool kDet, bool kMask>
+template <bool kBF16, bool kDet, bool kMask, bool kD64>
 cudaError_t launch_t(const BwdParams &p, cudaStream_t st) {
+  const int d = kD64 ? 64 : HD;
   TcMaps maps;
-  if (!make_map(&maps.q, p.q, p.total_q, p.n, BM, kBF16) ||
-      !make_map(&maps.dy, p.dy, p.total_q, p.n, BM, kBF16) ||
-      !make_map(&maps.k, p.k, p.total_kv, p.n_kv, BN, kBF16) ||
-      !make_map(&maps.v, p.v, p.total_kv, p.n_kv, BN, kBF16) ||
-      !make_map(&maps.dk, p.dk, p.total_kv, p.n_kv, BN, kBF16) ||
-      !make_map(&maps.dv, p.dv, p.total_kv, p.n_kv, BN, kBF16))
+  if (!make_map(&maps.q, p.q, p.total_q, p.n, d, BM, kBF16) ||
+      !make_map(&maps.dy, p.dy, p.total_q, p.n, d, BM, kBF16) ||
+      !make_map(&maps.k, p.k, p.total_kv, p.n_kv, d, BN, kBF16) ||
+      !make_map(&maps.v, p.v, p.total_kv, p.n_kv, d, BN, kBF16) ||
+      !make_map(&maps.dk, p.dk, p.total_kv, p.n_kv, d, BN, kBF16) ||
+      !make_map(&maps.dv, p.dv, p.total_kv, p.n_kv, d, BN, kBF16))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<kBF16, kDet, kMask>,
+  cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<kBF16, kDet, kMask, kD64>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   int dev = 0;
@@ -760,16 +775,23 @@ cudaError_t launch_t(const BwdParams &p, cudaStream_t st) {
   if ((e = cudaDeviceGetAttribute(&q.prefetch_ahead, cudaDevAttrMultiProcessorCount, dev)) !=
       cudaSuccess)
     return e;
-  bwd_tc_kernel<kBF16, kDet, kMask><<<p.n_items, NTHREADS, SMEM_BYTES, st>>>(q, maps);
+  bwd_tc_kernel<kBF16, kDet, kMask, kD64><<<p.n_items, NTHREADS, SMEM_BYTES, st>>>(q, maps);
   return cudaGetLastError();
+}
+
+template <bool kBF16, bool kD64>
+cudaError_t launch_dd(const BwdParams &p, cudaStream_t s) {
+  const bool mask = p.atten_mask != nullptr;
+  if (p.deterministic)
+    return mask ? launch_t<kBF16, true, true, kD64>(p, s) : launch_t<kBF16, true, false, kD64>(p, s);
+  return mask ? launch_t<kBF16, false, true, kD64>(p, s) : launch_t<kBF16, false, false, kD64>(p, s);
 }
 
 template <bool kBF16>
 cudaError_t launch_dt(const BwdParams &p, cudaStream_t s) {
-  const bool mask = p.atten_mask != nullptr;
-  if (p.deterministic)
-    return mask ? launch_t<kBF16, true, true>(p, s) : launch_t<kBF16, true, false>(p, s);
-  return mask ? launch_t<kBF16, false, true>(p, s) : launch_t<kBF16, false, false>(p, s);
+  if (p.d == 64) return launch_dd<kBF16, true>(p, s);
+  if (p.d == HD) return launch_dd<kBF16, false>(p, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -782,7 +804,7 @@ cudaError_t launch_wait_timeout_selftest(int32_t *err, long long timeout_ns, cud
 }
 
 bool tcgen05_supported(fa_dtype dt, int head_dim) {
-  return head_dim == HD && (dt == FA_DTYPE_BF16 || dt == FA_DTYPE_FP16);
+  return (head_dim == HD || head_dim == 64) && (dt == FA_DTYPE_BF16 || dt == FA_DTYPE_FP16);
 }
 
 cudaError_t launch_bwd_tcgen05(const BwdParams &p, fa_dtype dt, cudaStream_t s) {

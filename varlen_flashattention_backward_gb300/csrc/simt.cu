@@ -40,9 +40,11 @@ __device__ __forceinline__ float dot16(uint4 a, uint4 b) {
 }
 
 // Rows are read with 16-byte loads, D / (16 / sizeof(T)) lanes per row and
-// several rows per warp instruction; every load of a warp's rows is issued
-// before the reductions.  Needs 16-byte aligned dY and Y (the launcher
-// checks; otherwise preprocess_kernel below runs).
+// several rows per warp instruction.  The block first issues its dq_acc
+// zero stores, then every load of its rows (dY, Y and the statistics)
+// before any reduction, so that all its memory traffic is in flight at
+// once.  Needs 16-byte aligned dY and Y (the launcher checks; otherwise
+// preprocess_kernel below runs).
 template <typename T, int D>
 __global__ void __launch_bounds__(256) preprocess_vec_kernel(BwdParams p) {
   constexpr int kVec = 16 / int(sizeof(T));
@@ -58,15 +60,29 @@ __global__ void __launch_bounds__(256) preprocess_vec_kernel(BwdParams p) {
   const int sub = lane / kLanes, part = lane % kLanes;
   const uint4 *dy = static_cast<const uint4 *>(p.dy);
   const uint4 *y = static_cast<const uint4 *>(p.y);
+  for (int e = threadIdx.x; e < kQTile * (D / 4); e += 256) {
+    const int r = e / (D / 4), c4 = e % (D / 4);
+    const int i = row0 + r - s.qpad;
+    if (i < s.len_q)
+      reinterpret_cast<float4 *>(p.dq_acc + ((int64_t(s.cu_q) + i) * p.n + n) * D)[c4] =
+          make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   uint4 a[kPasses], c[kPasses];
+  float mm[kPasses], ll[kPasses];
 #pragma unroll
   for (int k = 0; k < kPasses; ++k) {
     const int i = row0 + warp * kRowsWarp + k * kRowsPass + sub - s.qpad;
     a[k] = c[k] = make_uint4(0u, 0u, 0u, 0u);
+    mm[k] = -CUDART_INF_F; ll[k] = 0.f;
     if (i < s.len_q) {
-      const int64_t e = ((int64_t(s.cu_q) + i) * p.n + n) * (D / kVec) + part;
+      const int64_t t = int64_t(s.cu_q) + i;
+      const int64_t e = (t * p.n + n) * (D / kVec) + part;
       a[k] = __ldg(dy + e);
       c[k] = __ldg(y + e);
+      if (part == 0) {
+        mm[k] = __ldg(p.smax + (t * p.n + n) * 8);
+        ll[k] = __ldg(p.ssum + (t * p.n + n) * 8);
+      }
     }
   }
 #pragma unroll
@@ -79,9 +95,7 @@ __global__ void __launch_bounds__(256) preprocess_vec_kernel(BwdParams p) {
     if (part == 0) {
       float lse2 = CUDART_INF_F;
       if (i < s.len_q) {
-        const int64_t t = int64_t(s.cu_q) + i;
-        const float m = p.smax[(t * p.n + n) * 8];
-        const float l = p.ssum[(t * p.n + n) * 8];
+        const float m = mm[k], l = ll[k];
         if (l > 0.f && m > -CUDART_INF_F) lse2 = (m + logf(l)) * kLog2e;
       } else {
         acc = 0.f;
@@ -89,13 +103,6 @@ __global__ void __launch_bounds__(256) preprocess_vec_kernel(BwdParams p) {
       p.lse2[int64_t(n) * p.tp + prow] = lse2;
       p.dsum[int64_t(n) * p.tp + prow] = acc;
     }
-  }
-  for (int e = threadIdx.x; e < kQTile * (D / 4); e += 256) {
-    const int r = e / (D / 4), c4 = e % (D / 4);
-    const int i = row0 + r - s.qpad;
-    if (i < s.len_q)
-      reinterpret_cast<float4 *>(p.dq_acc + ((int64_t(s.cu_q) + i) * p.n + n) * D)[c4] =
-          make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 
@@ -597,10 +604,10 @@ cudaError_t launch_pre_t(const BwdParams &p, cudaStream_t st) {
 
 template <typename T>
 cudaError_t launch_conv_t(const BwdParams &p, cudaStream_t st) {
-  const int64_t n = int64_t(p.total_q) * p.n * p.d;   // a multiple of 64 (D is 64 or 128)
+  const int64_t n = int64_t(p.total_q) * p.n * p.d;   // a multiple of 32 (D is)
   if ((reinterpret_cast<uintptr_t>(p.dq) & 15u) == 0) {
     int64_t blocks = (n / 8 + 255) / 256;
-    if (blocks > 152 * 8) blocks = 152 * 8;
+    if (blocks > 152 * 64) blocks = 152 * 64;
     if (blocks < 1) blocks = 1;
     dq_convert8_kernel<T><<<int(blocks), 256, 0, st>>>(p.dq_acc, static_cast<T *>(p.dq), n / 8,
                                                        p.scale);

@@ -129,6 +129,9 @@ def workload(cid: int, seed: int = 0) -> Workload:
         return Workload(5, "bf16", [16384] * 4, 16, 128, 4096, 0, keep_prob=0.9, seed=seed)
     if cid == 6:
         return Workload(6, "bf16", [2048] * 8, 16, 128, UNBOUNDED, 0, seed=seed)
+    if cid == 7:
+        # head dim 64: the bench mix with twice the heads (the same bytes)
+        return Workload(7, "bf16", [512, 1024, 2048, 512], 32, 64, UNBOUNDED, 0, seed=seed)
     raise ValueError(f"unknown workload {cid}")
 
 
