@@ -301,8 +301,14 @@ fa_status fa_gen_keep_mask(uint8_t *mask, int64_t nbits, uint64_t seed,
                            double keep_prob, fa_stream_t stream);
 
 /* Host-only introspection of the backward tile scheduler (no GPU needed).
- * Writes the work list the backward would run, in launch order, as 4 int32
- * per item: {sequence, key/value head, key tile, lo | count << 16}, meaning
+ * Writes the work list the backward would run, as 4 int32 per item:
+ * {sequence, key/value head, key tile, lo | count << 16}, in unit order:
+ * the items of each (sequence, head) unit together, longest first, units
+ * ordered by their longest item.  The backward launches the same items in
+ * this order, except that it sorts the last two waves (2 x SM count items)
+ * longest first, or the whole list when Q, dY, K, V and the fp32 dQ
+ * accumulator together fit in 85% of the device's L2; at head dim 64 the
+ * tensor-core kernel also pairs adjacent kv heads.  An item means
  * key rows [tile*kv_tile, tile*kv_tile + kv_tile) of that sequence and head
  * visit query tiles of 64 rows [lo, lo + count) of every query head of the
  * group.  kv_tile is 64 (CUDA-core kernel) or 128 (tcgen05 kernel).

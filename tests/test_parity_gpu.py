@@ -61,6 +61,9 @@ SMALL = {
     "d64_gqa_band_dropout": wl.Workload(21, "bf16", [300, 0, 150], 4, 64, 100, 20,
                                         keep_prob=0.8, seed=14, n_heads_kv=2),
     "d64_w7": wl.workload(7),
+    "d64_odd_kv_heads": wl.Workload(22, "bf16", [129, 0, 64, 250], 3, 64, BIG, 0, seed=15),
+    "d64_gqa_odd_kv_heads": wl.Workload(23, "bf16", [200, 77], 6, 64, 50, 5, seed=16,
+                                        n_heads_kv=3),
     "d96_causal_gqa_fp16": wl.Workload(17, "fp16", [77, 130], 4, 96, BIG, 0, seed=10,
                                        n_heads_kv=2),
     "d192_dropout": wl.Workload(18, "bf16", [66, 129], 2, 192, BIG, BIG, keep_prob=0.85,

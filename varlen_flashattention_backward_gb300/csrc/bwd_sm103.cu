@@ -190,10 +190,13 @@ __device__ __forceinline__ bool wait_or_abort(const Ctl &c, uint32_t bar, uint32
 // kMask: an explicit attention mask is read.  Each is a separate
 // instantiation so that the default kernel carries none of its code (the
 // mask's untaken branch alone cost 5-10% of the default kernel's time).
-// kD64: head dim 64.  Only the first 64-column box of each tile is loaded;
-// S^T and dP^T take 4 k-steps and dV, dK are N = 64 products.  dQ^T keeps
-// M = 128 (d) with the second K box zeroed, so its rows 64-127 are zero
-// and are not reduced.
+// kD64: head dim 64.  An item may cover two adjacent kv heads (the upper
+// half of WorkItem::head holds the extra head count): their K and V fill the
+// two 64-column boxes of the tiles, their dV and dK the two halves of the
+// accumulators, and the loop runs over the query heads of both.  Q and dY
+// load one box; S^T and dP^T take 4 k-steps and dV, dK are N = 64
+// products.  dQ^T keeps M = 128 (d) starting at the item's own K box, so
+// its rows 64-127 (the other box, or zeros) are not reduced.
 template <bool kBF16, bool kDet, bool kMask, bool kD64>
 __global__ void __launch_bounds__(NTHREADS, 1)
     bwd_tc_kernel(const BwdParams p, const __grid_constant__ TcMaps maps) {
@@ -246,10 +249,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tmem_relinquish();
   }
   if constexpr (kD64) {
-    // The second K box (d 64-127) feeds the M = 128 dQ^T product: zero it.
-    for (uint32_t o = threadIdx.x * 16u; o < 16384u; o += NTHREADS * 16u)
-      st_shared_v4(sb + SM_K + 16384u + o, 0u, 0u, 0u, 0u);
-    fence_proxy_async_smem();
+    // With one kv head the second K box (rows 64-127 of the M = 128 dQ^T
+    // product) is not loaded: zero it.
+    if (kDet || (item_by_grid.head >> 16) == 0) {
+      for (uint32_t o = threadIdx.x * 16u; o < 16384u; o += NTHREADS * 16u)
+        st_shared_v4(sb + SM_K + 16384u + o, 0u, 0u, 0u, 0u);
+      fence_proxy_async_smem();
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -257,11 +263,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t tmem = s_tmem;
   const WorkItem item = kDet ? p.items[s_item] : item_by_grid;
   const SeqInfo sq = p.seqs[item.seq];
-  const int kvh = item.head;
+  const int kvh = item.head & 0xFFFF;
+  const int nh = kD64 ? 1 + (item.head >> 16) : 1;   // kv heads of this item
   const int group = p.n / p.n_kv;
   const int k0 = item.tile * BN;
   const int qlo = item_lo(item), qcnt = item_count(item);
-  const int n_it = qcnt * group;
+  const int per_head = qcnt * group;   // iterations per kv head
+  const int n_it = per_head * nh;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -275,8 +283,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       __syncwarp();
       const int ky = sq.cu_k + k0, kx = kvh * DD;
-      mbar_arrive_expect_tx_w(bar(B_KV), 2 * NBOX * 16384);
-      for (int bx = 0; bx < NBOX; ++bx) {
+      const int kvbox = kD64 ? nh : NBOX;
+      mbar_arrive_expect_tx_w(bar(B_KV), 2 * kvbox * 16384);
+      for (int bx = 0; bx < kvbox; ++bx) {
         tma_load_2d_w(sb + SM_K + bx * 16384, &maps.k, bar(B_KV), kx + 64 * bx, ky);
         tma_load_2d_w(sb + SM_V + bx * 16384, &maps.v, bar(B_KV), kx + 64 * bx, ky);
       }
@@ -284,8 +293,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // some SM about when this one ends: bring its K and V into L2 now.
       if (lane == 0 && blockIdx.x + p.prefetch_ahead < p.n_items) {
         const WorkItem nx = p.items[blockIdx.x + p.prefetch_ahead];
-        const int nky = p.seqs[nx.seq].cu_k + nx.tile * BN, nkx = nx.head * DD;
-        for (int bx = 0; bx < NBOX; ++bx) {
+        const int nky = p.seqs[nx.seq].cu_k + nx.tile * BN, nkx = (nx.head & 0xFFFF) * DD;
+        for (int bx = 0; bx < (kD64 ? 1 + (nx.head >> 16) : NBOX); ++bx) {
           tma_prefetch_l2_2d(&maps.k, nkx + 64 * bx, nky);
           tma_prefetch_l2_2d(&maps.v, nkx + 64 * bx, nky);
         }
@@ -349,9 +358,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           // D[128 x 64] = A[128 x 128] B[64 x 128]^T, both K-major (2 boxes along K)
           const uint64_t bq = sdesc_sw128(sb + SM_Q + st * 16384, 16, 1024);
           const uint64_t by = sdesc_sw128(sb + SM_DY + st * 16384, 16, 1024);
+          const uint32_t mo = kD64 ? uint32_t(((L / per_head) * 16384) >> 4) : 0u;  // kv head box
 #pragma unroll
           for (int kk = 0; kk < DD / 16; ++kk) {
-            const uint32_t ao = (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+            const uint32_t ao = (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4) + mo;
             const uint32_t bo = (((kk >> 2) * 8192 + (kk & 3) * 32) >> 4);
             const uint32_t acc = kk > 0 ? 1u : 0u;
             mma_ss_w(tmem + COL_S, dk_ + ao, bq + bo, id_s, acc);
@@ -367,7 +377,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         bool ok = wait_or_abort(ctl, bar(B_KV), 0, ROLE_MMA);
         for (int L = 0; ok && L < n_it; ++L) {
           const int st = L % STAGES;
-          const uint32_t acc0 = L > 0 ? 1u : 0u;
+          const int m = kD64 ? L / per_head : 0;                  // kv head of the item
+          const uint32_t acc0 = (kD64 ? L - m * per_head : L) > 0 ? 1u : 0u;
+          const uint32_t mcol = uint32_t(m * 64);                  // its accumulator half
+          const uint32_t mo = uint32_t((m * 16384) >> 4);          // its K box
           if (!(ok = wait_or_abort(ctl, bar(B_PFULL), L & 1, ROLE_MMA))) break;
           tc_fence_after();
           {
@@ -375,7 +388,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const uint64_t b0 = sdesc_sw128(sb + SM_DY + st * 16384, 8192, 1024);
 #pragma unroll
             for (int kk = 0; kk < BM / 16; ++kk)
-              mma_ts_w(tmem + COL_DV, tmem + COL_P + kk * 8, b0 + ((kk * 2048) >> 4), id_g,
+              mma_ts_w(tmem + COL_DV + mcol, tmem + COL_P + kk * 8, b0 + ((kk * 2048) >> 4), id_g,
                        kk > 0 ? 1u : acc0);
           }
           mma_commit_w(bar(B_PFREE));
@@ -388,11 +401,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const uint64_t b0 = sdesc_sw128(sb + SM_Q + st * 16384, 8192, 1024);
 #pragma unroll
             for (int kk = 0; kk < BM / 16; ++kk) {
-              mma_ts_w(tmem + COL_DK, tmem + COL_DS + kk * 8, b0 + ((kk * 2048) >> 4), id_g,
+              mma_ts_w(tmem + COL_DK + mcol, tmem + COL_DS + kk * 8, b0 + ((kk * 2048) >> 4), id_g,
                        kk > 0 ? 1u : acc0);
-              mma_ss_w(tmem + COL_DQ, dkt + (((2 * kk) * 2048) >> 4),
+              mma_ss_w(tmem + COL_DQ, dkt + mo + (((2 * kk) * 2048) >> 4),
                        dds + (((2 * kk) * 2048) >> 4), id_q, kk > 0 ? 1u : 0u);
-              mma_ss_w(tmem + COL_DQ, dkt + (((2 * kk + 1) * 2048) >> 4),
+              mma_ss_w(tmem + COL_DQ, dkt + mo + (((2 * kk + 1) * 2048) >> 4),
                        dds + (((2 * kk + 1) * 2048) >> 4), id_q, 1u);
             }
           }
@@ -550,7 +563,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint32_t col = half == 0 ? COL_DV : COL_DK;
       const uint32_t stage = sb + (half == 0 ? SM_Q : SM_DY);
 #pragma unroll 1
-      for (int c0 = 0; c0 < DD; c0 += 32) {
+      for (int c0 = 0; c0 < DD * nh; c0 += 32) {
         uint32_t r[32];
         if (n_it > 0) {
           tmem_ld32(tmem + lane_off + col + c0, r);
@@ -580,7 +593,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           wait_or_abort(ctl, bar(B_EPI + half), 0, ROLE_EPILOGUE)) {
         const CUtensorMap *m = half == 0 ? &maps.dv : &maps.dk;
         const int y = sq.cu_k + k0, x = kvh * DD;
-        for (int bx = 0; bx < NBOX; ++bx) tma_store_2d(m, stage + bx * 16384, x + 64 * bx, y);
+        for (int bx = 0; bx < (kD64 ? nh : NBOX); ++bx)
+          tma_store_2d(m, stage + bx * 16384, x + 64 * bx, y);
         bulk_commit_group();
         bulk_wait_group_read0();
       }
@@ -590,9 +604,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const float sc = half == 0 ? 1.f : p.scale;
       const uint32_t col = half == 0 ? COL_DV : COL_DK;
       const bool valid = jg < sq.len_k;
-      T *rowp = out + ((int64_t(sq.cu_k) + jg) * p.n_kv + kvh) * DD;
+      T *rowp = out + ((int64_t(sq.cu_k) + jg) * p.n_kv + kvh) * DD;   // nh heads adjacent
 #pragma unroll 1
-      for (int c0 = 0; c0 < DD; c0 += 32) {
+      for (int c0 = 0; c0 < DD * nh; c0 += 32) {
         uint32_t r[32];
         if (n_it > 0) {
           tmem_ld32(tmem + lane_off + col + c0, r);
