@@ -62,7 +62,7 @@
  *                      to total_q / total_kv, total_q > 1M, head_num not a
  *                      multiple of head_num_kv, unknown dtype, non-finite
  *                      scale, drop_mask_bytes too small
- *   FA_ERR_UNSUPPORTED a valid request this build does not implement:
+ *   FA_ERR_UNSUPPORTED a valid request this library does not implement:
  *                      head_dim not in {32, 64, 96, 128, 192} (the
  *                      tensor-core backward takes 64 and 128 in 16-bit
  *                      types; the rest run on the CUDA-core kernels),

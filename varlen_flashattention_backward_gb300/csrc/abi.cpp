@@ -103,8 +103,8 @@ fa_status check_problem(Problem &pr, const char *layout,
   for (int64_t b = 0; b < pr.batch; ++b)
     if ((pr.q_start && pr.q_start[b] < 0) || (pr.kv_start && pr.kv_start[b] < 0))
       return FA_ERR_INVALID;
-  // sparseMode: 0..8, 5 not supported (parameter table); this build
-  // implements the window modes 0, 2, 3 and 4.
+  // sparseMode: 0..8, 5 not supported (parameter table); this library
+  // implements modes 0-4 (the window modes and the explicit mask).
   if (pr.sparse_mode < 0 || pr.sparse_mode > 8 || pr.sparse_mode == 5) return FA_ERR_INVALID;
   if (pr.sparse_mode > 4) return FA_ERR_UNSUPPORTED;
   if (pr.atten_mask != nullptr) {
@@ -399,7 +399,7 @@ const char *fa_status_string(fa_status s) {
     case FA_ERR_NULLPTR: return "FA_ERR_NULLPTR: a required pointer is null";
     case FA_ERR_INVALID: return "FA_ERR_INVALID: an argument is out of range";
     case FA_ERR_UNSUPPORTED:
-      return "FA_ERR_UNSUPPORTED: valid request not implemented by this build";
+      return "FA_ERR_UNSUPPORTED: valid request not implemented by this library";
     case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace too small";
     case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call failed";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a bounded in-kernel wait expired";

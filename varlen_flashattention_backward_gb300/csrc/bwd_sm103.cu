@@ -1,5 +1,5 @@
 // Backward of varlen attention on the sm_103a tensor cores (tcgen05 + TMEM +
-// TMA), head_dim 128, bf16 or fp16 storage.
+// TMA), head_dim 128 (and 64, see kD64 below), bf16 or fp16 storage.
 //
 // It computes the FAG-V2 page's backward (aclnnFlashAttentionUnpaddingScoreGradV2,
 // section 功能说明 / 计算公式: dV = P^T dY, dQ = dS K / sqrt(d),
