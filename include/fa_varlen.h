@@ -320,6 +320,24 @@ fa_status fa_varlen_bwd_schedule(const int64_t *seq_lens_q, const int64_t *seq_l
                                  int64_t next_tokens, int32_t kv_tile, int32_t *items,
                                  int64_t capacity, int64_t *n_items);
 
+/* fa_varlen_bwd_schedule with the launch-time ordering made explicit, as
+ * the backward applies it: head_num, head_dim and dtype size the working
+ * set (Q, dY, K, V and the fp32 dQ accumulator); when it fits in 85% of
+ * l2_bytes the whole list is sorted longest first, else the last
+ * tail_items items are (the backward passes the device's L2 size and twice
+ * its SM count; 0 turns either off).  head_pairs != 0 groups two adjacent
+ * kv heads per item (WorkItem head field: first | (count - 1) << 16), as
+ * the tensor-core kernel does at head_dim 64.  An item's "length" for the
+ * sorts is its query-tile count times its head count.  Errors as for
+ * fa_varlen_bwd_schedule, plus FA_ERR_INVALID for head_num, head_dim or
+ * dtype out of range and negative l2_bytes / tail_items. */
+fa_status fa_varlen_bwd_schedule_ex(const int64_t *seq_lens_q, const int64_t *seq_lens_kv,
+                                    int64_t batch, int64_t head_num, int64_t head_num_kv,
+                                    int64_t head_dim, fa_dtype dtype, int64_t pre_tokens,
+                                    int64_t next_tokens, int32_t kv_tile, int64_t l2_bytes,
+                                    int64_t tail_items, int32_t head_pairs, int32_t *items,
+                                    int64_t capacity, int64_t *n_items);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int32_t fa_varlen_version(void);
 

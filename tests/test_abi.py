@@ -266,3 +266,86 @@ def test_negative_chunk_start_is_invalid():
                                    fa._DTYPE[torch.float32], b"TND", 0.125, 1.0, BIG, BIG, 0,
                                    fake, fake, fake, fake, 1 << 20, None, ctypes.byref(fo))
     assert st == fa.FA_ERR_INVALID
+
+
+# ---------------------------------------------------------------------------
+# launch-order rules of the scheduler (fa_varlen_bwd_schedule_ex)
+# ---------------------------------------------------------------------------
+
+ORDER_CASES = [
+    ([512, 1024, 2048, 512], 16, 16, 128, BIG, 0),
+    ([37, 64, 0, 1, 129, 700], 4, 2, 128, 100, 20),
+    ([300, 200, 1000], 6, 3, 64, BIG, 0),
+]
+
+
+def _item_key(it):
+    s_, h, nh, t, lo, cnt = it
+    return (s_, h, nh, t, lo, cnt)
+
+
+def _length(it):
+    return it[5] * it[2]
+
+
+@pytest.mark.parametrize("case", ORDER_CASES)
+def test_whole_list_longest_first_when_it_fits_in_l2(case):
+    lens, n, nkv, d, pre, nxt = case
+    unit = fa.bwd_schedule_ex(lens, lens, n, nkv, d, torch.bfloat16, pre, nxt, 128)
+    fit = fa.bwd_schedule_ex(lens, lens, n, nkv, d, torch.bfloat16, pre, nxt, 128,
+                             l2_bytes=1 << 40)
+    small = fa.bwd_schedule_ex(lens, lens, n, nkv, d, torch.bfloat16, pre, nxt, 128,
+                               l2_bytes=1 << 10)
+    assert sorted(map(_item_key, fit)) == sorted(map(_item_key, unit))
+    lengths = [_length(it) for it in fit]
+    assert lengths == sorted(lengths, reverse=True)
+    # stable: equal lengths keep their unit order
+    pos = {_item_key(it): i for i, it in enumerate(unit)}
+    for a, b in zip(fit, fit[1:]):
+        if _length(a) == _length(b):
+            assert pos[_item_key(a)] < pos[_item_key(b)]
+    # a working set larger than L2 keeps unit order
+    assert small == unit
+
+
+@pytest.mark.parametrize("tail", [1, 5, 40, 10**6])
+def test_tail_of_the_unit_order_is_sorted(tail):
+    lens, n, nkv, d, pre, nxt = ORDER_CASES[1]
+    unit = fa.bwd_schedule_ex(lens, lens, n, nkv, d, torch.bfloat16, pre, nxt, 128)
+    got = fa.bwd_schedule_ex(lens, lens, n, nkv, d, torch.bfloat16, pre, nxt, 128,
+                             tail_items=tail)
+    k = len(unit) if tail >= len(unit) else tail
+    if tail >= len(unit):
+        assert got == unit     # no tail sort when the tail would be the whole list
+        return
+    assert got[:-k] == unit[:-k]
+    assert sorted(map(_item_key, got[-k:])) == sorted(map(_item_key, unit[-k:]))
+    lengths = [_length(it) for it in got[-k:]]
+    assert lengths == sorted(lengths, reverse=True)
+
+
+@pytest.mark.parametrize("nkv", [1, 2, 3, 8])
+def test_head_pairs_cover_every_kv_head_once(nkv):
+    lens = [300, 0, 129, 64]
+    single = fa.bwd_schedule_ex(lens, lens, 2 * nkv, nkv, 64, torch.bfloat16, BIG, 0, 128)
+    pairs = fa.bwd_schedule_ex(lens, lens, 2 * nkv, nkv, 64, torch.bfloat16, BIG, 0, 128,
+                               head_pairs=True)
+    assert len(pairs) == sum((L + 127) // 128 for L in lens) * ((nkv + 1) // 2)
+    covered = []
+    for s_, h, nh, t, lo, cnt in pairs:
+        assert h % 2 == 0 and nh == min(2, nkv - h)
+        for hh in range(h, h + nh):
+            covered.append((s_, hh, t, lo, cnt))
+    assert sorted(covered) == sorted((s_, h, t, lo, cnt) for s_, h, nh, t, lo, cnt in single)
+
+
+def test_schedule_ex_argument_checks():
+    L = fa.lib()
+    lq = (ctypes.c_int64 * 2)(37, 64)
+    n = ctypes.c_int64(0)
+    ok = (lq, lq, 2, 4, 2, 128, 2, BIG, BIG, 128, 0, 0, 0, None, 0, ctypes.byref(n))
+    assert L.fa_varlen_bwd_schedule_ex(*ok) == fa.FA_OK
+    for i, v in ((3, 3), (5, 1000), (6, 7), (10, -1), (11, -1), (9, 32)):
+        bad = list(ok)
+        bad[i] = v
+        assert L.fa_varlen_bwd_schedule_ex(*bad) == fa.FA_ERR_INVALID, (i, v)

@@ -79,6 +79,9 @@ _SIGS = {
     "fa_varlen_selftest_wait_timeout": ([_vp, _sz, _i64, _vp], _i32),
     "fa_varlen_bwd_schedule": ([_pi64, _pi64, _i64, _i64, _i64, _i64, _i32,
                                 ctypes.POINTER(ctypes.c_int32), _i64, _pi64], _i32),
+    "fa_varlen_bwd_schedule_ex": ([_pi64, _pi64, _i64, _i64, _i64, _i64, _i32, _i64, _i64, _i32,
+                                   _i64, _i64, _i32, ctypes.POINTER(ctypes.c_int32), _i64, _pi64],
+                                  _i32),
 }
 
 EXPORTS = tuple(_SIGS)
@@ -321,6 +324,27 @@ def bwd_schedule(lens_q, lens_kv, n_kv, pre_tokens, next_tokens, kv_tile):
     for i in range(n.value):
         s, h, t, r = buf[4 * i:4 * i + 4]
         out.append((s, h, t, r & 0xFFFF, (r >> 16) & 0xFFFF))
+    return out
+
+
+def bwd_schedule_ex(lens_q, lens_kv, n, n_kv, d, dtype, pre_tokens, next_tokens, kv_tile,
+                    l2_bytes=0, tail_items=0, head_pairs=False):
+    """fa_varlen_bwd_schedule_ex: the work list in launch order, as a list of
+    (seq, first kv head, kv heads, kv_tile, q_lo, q_count)."""
+    lq, b, _ = _lens(lens_q)
+    lk, _, _ = _lens(lens_kv)
+    cnt = ctypes.c_int64(0)
+    args = (lq, lk, b, n, n_kv, d, _DTYPE[dtype], pre_tokens, next_tokens, kv_tile,
+            int(l2_bytes), int(tail_items), int(bool(head_pairs)))
+    _check(lib().fa_varlen_bwd_schedule_ex(*args, None, 0, ctypes.byref(cnt)),
+           "fa_varlen_bwd_schedule_ex")
+    buf = (ctypes.c_int32 * max(4, 4 * cnt.value))()
+    _check(lib().fa_varlen_bwd_schedule_ex(*args, buf, cnt.value, ctypes.byref(cnt)),
+           "fa_varlen_bwd_schedule_ex")
+    out = []
+    for i in range(cnt.value):
+        s_, h, t, r = buf[4 * i:4 * i + 4]
+        out.append((s_, h & 0xFFFF, 1 + (h >> 16), t, r & 0xFFFF, (r >> 16) & 0xFFFF))
     return out
 
 

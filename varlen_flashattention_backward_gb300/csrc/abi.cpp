@@ -691,25 +691,46 @@ fa_status fa_varlen_read_error(const void *workspace, size_t workspace_bytes, fa
   return word == 0 ? FA_OK : FA_ERR_TIMEOUT;
 }
 
-fa_status fa_varlen_bwd_schedule(const int64_t *seq_lens_q, const int64_t *seq_lens_kv,
-                                 int64_t batch, int64_t head_num_kv, int64_t pre_tokens,
-                                 int64_t next_tokens, int32_t kv_tile, int32_t *items,
-                                 int64_t capacity, int64_t *n_items) {
+fa_status fa_varlen_bwd_schedule_ex(const int64_t *seq_lens_q, const int64_t *seq_lens_kv,
+                                    int64_t batch, int64_t head_num, int64_t head_num_kv,
+                                    int64_t head_dim, fa_dtype dtype, int64_t pre_tokens,
+                                    int64_t next_tokens, int32_t kv_tile, int64_t l2_bytes,
+                                    int64_t tail_items, int32_t head_pairs, int32_t *items,
+                                    int64_t capacity, int64_t *n_items) {
   if (seq_lens_q == nullptr || seq_lens_kv == nullptr || n_items == nullptr) return FA_ERR_NULLPTR;
   if (capacity > 0 && items == nullptr) return FA_ERR_NULLPTR;
-  if (batch < 1 || batch > kMaxBatch || head_num_kv < 1 || head_num_kv > 256) return FA_ERR_INVALID;
+  if (batch < 1 || batch > kMaxBatch || head_num_kv < 1 || head_num_kv > 256 || head_num < 1 ||
+      head_num > 256 || head_num % head_num_kv != 0 || head_dim < 1 || head_dim > 768 ||
+      l2_bytes < 0 || tail_items < 0)
+    return FA_ERR_INVALID;
+  if (dtype != FA_DTYPE_FP32 && dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16)
+    return FA_ERR_INVALID;
   if (kv_tile != kSimtKvTile && kv_tile != kTcKvTile) return FA_ERR_INVALID;
-  for (int64_t b = 0; b < batch; ++b)
+  int64_t tq = 0, tk = 0;
+  for (int64_t b = 0; b < batch; ++b) {
     if (seq_lens_q[b] < 0 || seq_lens_kv[b] < 0 || seq_lens_q[b] > (int64_t(1) << 20) ||
         seq_lens_kv[b] > (int64_t(1) << 20))
       return FA_ERR_INVALID;
-  Problem pr{seq_lens_q, seq_lens_kv, batch, 0, 0, head_num_kv, head_num_kv, 128,
-             FA_DTYPE_BF16, 1.0, pre_tokens, next_tokens, 0, 0, 0};
-  auto list = build_bwd_items(pr, kv_tile, false);
+    tq += seq_lens_q[b];
+    tk += seq_lens_kv[b];
+  }
+  Problem pr{seq_lens_q, seq_lens_kv, batch, tq, tk, head_num, head_num_kv, head_dim,
+             dtype, 1.0, pre_tokens, next_tokens, 0, 0, 0};
+  auto list = build_bwd_items(pr, kv_tile, false, size_t(l2_bytes), head_pairs != 0,
+                              size_t(tail_items));
   *n_items = int64_t(list.size());
   const int64_t m = std::min<int64_t>(capacity, int64_t(list.size()));
   if (m > 0) std::memcpy(items, list.data(), size_t(m) * sizeof(WorkItem));
   return FA_OK;
+}
+
+fa_status fa_varlen_bwd_schedule(const int64_t *seq_lens_q, const int64_t *seq_lens_kv,
+                                 int64_t batch, int64_t head_num_kv, int64_t pre_tokens,
+                                 int64_t next_tokens, int32_t kv_tile, int32_t *items,
+                                 int64_t capacity, int64_t *n_items) {
+  return fa_varlen_bwd_schedule_ex(seq_lens_q, seq_lens_kv, batch, head_num_kv, head_num_kv, 128,
+                                   FA_DTYPE_BF16, pre_tokens, next_tokens, kv_tile, 0, 0, 0,
+                                   items, capacity, n_items);
 }
 
 fa_status fa_varlen_selftest_wait_timeout(void *workspace, size_t workspace_bytes,
