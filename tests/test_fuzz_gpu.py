@@ -1,4 +1,4 @@
-"""Seeded random problems through the tensor-core backward against the fp64
+"""Seeded random problems through both backward kernels against the fp64
 oracle: element types, head dims 64 and 128, grouped heads, ragged and
 empty sequences, Lq != Lk, windows of every sparse mode, explicit masks,
 dropout, outer-split starts and the deterministic mode, in combination.
@@ -28,7 +28,7 @@ def built():
     torch.cuda.set_device(DEV)
 
 
-def _case(seed):
+def _case(seed, dims=(64, 128), dtypes=("bf16", "fp16")):
     g = np.random.default_rng(1000 + seed)
     b = int(g.integers(1, 5))
     lens = [int(x) for x in g.integers(0, 300, b)]
@@ -36,8 +36,8 @@ def _case(seed):
     lens_kv = lens if g.random() < 0.5 else [int(x) for x in g.integers(1, 300, b)]
     n_kv = int(g.choice([1, 2, 3]))
     n = n_kv * int(g.choice([1, 2]))
-    d = int(g.choice([64, 128]))
-    dtype = str(g.choice(["bf16", "fp16"]))
+    d = int(g.choice(list(dims)))
+    dtype = str(g.choice(list(dtypes)))
     mode = int(g.choice([0, 0, 1, 2, 3, 4]))
     pre = int(g.choice([BIG, int(g.integers(0, 200))]))
     nxt = int(g.choice([BIG, 0, int(g.integers(0, 50))]))
@@ -54,9 +54,7 @@ def _case(seed):
     return w, mode, am, qs, ks, det
 
 
-@pytest.mark.parametrize("seed", range(24))
-def test_random_problem_against_oracle(seed):
-    w, mode, am_np, qs, ks, det = _case(seed)
+def _run_case(w, mode, am_np, qs, ks, det, impl):
     tensors = wl.make_tensors(w)
     mask_np = wl.make_keep_mask(w)
     mask = None if mask_np is None else torch.from_numpy(mask_np).to(DEV)
@@ -66,10 +64,10 @@ def test_random_problem_against_oracle(seed):
                      w.keep_prob, mask, q_start=qs, kv_start=ks, sparse_mode=mode, atten_mask=am)
     ws = torch.empty(fa.bwd_workspace_size(w.lens, w.lens_kv, w.n_heads, w.n_heads_kv,
                                            w.head_dim, q.dtype, w.keep_prob, w.pre_tokens,
-                                           w.next_tokens, fa.FA_BWD_TCGEN05, mode, am),
+                                           w.next_tokens, impl, mode, am),
                      dtype=torch.uint8, device=DEV)
     dq, dk, dv = fa.bwd(q, k, v, dy, y, m, l, w.lens, w.lens_kv, w.scale, w.pre_tokens,
-                        w.next_tokens, w.keep_prob, mask, workspace=ws, impl=fa.FA_BWD_TCGEN05,
+                        w.next_tokens, w.keep_prob, mask, workspace=ws, impl=impl,
                         deterministic=det, q_start=qs, kv_start=ks, sparse_mode=mode,
                         atten_mask=am)
     torch.cuda.synchronize()
@@ -84,3 +82,15 @@ def test_random_problem_against_oracle(seed):
                                            sparse_mode=mode, atten_mask=am_np)
     assert_close(dict(y=y, dq=dq, dk=dk, dv=dv), dict(y=ry, dq=rdq, dk=rdk, dv=rdv),
                  TOL[w.dtype])
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_problem_tcgen05(seed):
+    _run_case(*_case(seed), fa.FA_BWD_TCGEN05)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_problem_cuda_cores(seed):
+    """The CUDA-core kernel: every element type and every head dim it has."""
+    _run_case(*_case(100 + seed, dims=(32, 64, 96, 128, 192), dtypes=("fp32", "bf16", "fp16")),
+              fa.FA_BWD_SIMT)
