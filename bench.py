@@ -57,9 +57,43 @@ def allowed_pairs(lens_q, lens_kv, pre, nxt) -> int:
     return total
 
 
-def workload_flops(w) -> float:
-    return 10.0 * w.head_dim * w.n_heads * allowed_pairs(w.lens, w.lens_kv, w.pre_tokens,
-                                                         w.next_tokens)
+def seq_window(w, b):
+    """(pre, next) of sequence b on chunk-local indices, by the library's
+    rule: the sparse mode's window on global positions (modes 1-3 ignore
+    preTokens / nextTokens; 2 is the top-left, 3 the bottom-right lower
+    triangle), shifted by the outer-split starts, clamped to +-2^28."""
+    lim = 1 << 28
+    clamp = lambda x: max(-lim, min(lim, x))  # noqa: E731
+    mode = getattr(w, "sparse_mode", 0)
+    pre = lim if mode in (1, 2, 3) else clamp(w.pre_tokens)
+    nxt = {1: lim, 2: 0, 3: w.lens_kv[b] - w.lens[b]}.get(mode, clamp(w.next_tokens))
+    qs = w.q_start[b] if getattr(w, "q_start", None) else 0
+    ks = w.kv_start[b] if getattr(w, "kv_start", None) else 0
+    return clamp(pre - (qs - ks)), clamp(nxt + (qs - ks))
+
+
+def workload_pairs(w, atten_mask=None) -> int:
+    """Allowed (query, key) pairs of one head over the batch: the window of
+    each sequence, and where an explicit mask applies (modes 0, 1, 4), its
+    unmasked entries."""
+    mode = getattr(w, "sparse_mode", 0)
+    total = 0
+    for b, (lq, lk) in enumerate(zip(w.lens, w.lens_kv)):
+        pre, nxt = seq_window(w, b)
+        if atten_mask is None or mode not in (0, 1, 4):
+            total += allowed_pairs([lq], [lk], pre, nxt)
+            continue
+        if lq == 0 or lk == 0:
+            continue
+        i = np.arange(lq)[:, None]
+        j = np.arange(lk)[None, :]
+        ok = (j >= i - pre) & (j <= i + nxt) & (atten_mask[:lq, :lk] == 0)
+        total += int(ok.sum())
+    return total
+
+
+def workload_flops(w, atten_mask=None) -> float:
+    return 10.0 * w.head_dim * w.n_heads * workload_pairs(w, atten_mask)
 
 
 def measured_peaks():
@@ -228,6 +262,10 @@ def run_reference(args, w):
     if rank != 0:
         return 0
     from varlen_flashattention_backward_gb300 import workloads as wl
+    if w.sparse_mode or w.q_start is not None or w.mask_density > 0:
+        print(json.dumps({"impl": "reference", "unavailable": "the oracle sample covers "
+                          "plain-window workloads (sparse mode 0, no starts, no mask)"}))
+        return 0
     tensors = wl.make_tensors(w)
     per_step = []
     # keep the whole run to about two minutes of CPU work
@@ -280,12 +318,17 @@ def run_cuda(args, w):
     mask = None
     if w.keep_prob < 1.0:
         mask = fa.gen_keep_mask(w.mask_bits, w.mask_seed, w.keep_prob, device=dev)
+    am_np = wl.make_atten_mask(w)
+    am = None if am_np is None else torch.from_numpy(am_np).to(dev)
+    extra = dict(q_start=w.q_start, kv_start=w.kv_start, sparse_mode=w.sparse_mode,
+                 atten_mask=am)
     y, smax, ssum = fa.fwd(q, k, v, w.lens, w.lens_kv, w.scale, w.pre_tokens, w.next_tokens,
-                           w.keep_prob, mask)
+                           w.keep_prob, mask, **extra)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     impl = {"auto": fa.FA_BWD_AUTO, "simt": fa.FA_BWD_SIMT, "tcgen05": fa.FA_BWD_TCGEN05}[args.kernel]
     ws_bytes = fa.bwd_workspace_size(w.lens, w.lens_kv, w.n_heads, w.n_heads_kv, w.head_dim,
-                                     q.dtype, w.keep_prob, w.pre_tokens, w.next_tokens, impl)
+                                     q.dtype, w.keep_prob, w.pre_tokens, w.next_tokens, impl,
+                                     w.sparse_mode, am)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -293,7 +336,8 @@ def run_cuda(args, w):
     def step(events=None):
         fa.bwd(q, k, v, dy, y, smax, ssum, w.lens, w.lens_kv, w.scale, w.pre_tokens,
                w.next_tokens, w.keep_prob, mask, dq=dq, dk=dk, dv=dv, workspace=ws,
-               stream=stream, impl=impl, events=events)
+               stream=stream, impl=impl, events=events, deterministic=args.deterministic,
+               **extra)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -329,7 +373,7 @@ def run_cuda(args, w):
     pre_ms = [e[1].elapsed_time(e[2]) for e in evs]
     conv_ms = [e[3].elapsed_time(e[4]) for e in evs]
     total_ms = max_over_ranks(sum(step_ms), world, dev)
-    flops = workload_flops(w)
+    flops = workload_flops(w, am_np)
     value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
 
     # end to end through the public API: every step copies its inputs from
@@ -341,7 +385,8 @@ def run_cuda(args, w):
     # the kernels of step i.  The timed region runs from before the first
     # input copy to the end of the last output copy.  The same steps run
     # back to back without overlap give `serial_value`.
-    src_in = (q, k, v, dy, y, smax, ssum) + ((mask,) if mask is not None else ())
+    src_in = ((q, k, v, dy, y, smax, ssum) + ((mask,) if mask is not None else ()) +
+              ((am,) if am is not None else ()))
     host_in = [t.cpu().pin_memory() for t in src_in]
     host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
     dev_in = [[torch.empty_like(t) for t in src_in] for _ in range(2)]
@@ -352,11 +397,13 @@ def run_cuda(args, w):
 
     def e2e_bwd(bi):
         x = dev_in[bi]
+        xm = x[7] if mask is not None else None
+        xa = x[-1] if am is not None else None
         return fa.bwd(x[0], x[1], x[2], x[3], x[4], x[5], x[6], w.lens, w.lens_kv, w.scale,
-                      w.pre_tokens, w.next_tokens, w.keep_prob,
-                      x[7] if mask is not None else None, dq=dev_out[bi][0],
+                      w.pre_tokens, w.next_tokens, w.keep_prob, xm, dq=dev_out[bi][0],
                       dk=dev_out[bi][1], dv=dev_out[bi][2], workspace=ws, stream=stream,
-                      impl=impl)
+                      impl=impl, deterministic=args.deterministic, q_start=w.q_start,
+                      kv_start=w.kv_start, sparse_mode=w.sparse_mode, atten_mask=xa)
 
     def e2e_run(n, overlap):
         """n steps; returns the elapsed milliseconds."""
@@ -422,7 +469,9 @@ def run_cuda(args, w):
     traffic = profile_traffic(f"{kernel_tag}_w{w.cid}", source_digest())
 
     cpu = None
-    if not args.no_cpu_baseline:
+    # the oracle sample times plain-window units only
+    plain = w.sparse_mode == 0 and w.q_start is None and am_np is None
+    if not args.no_cpu_baseline and plain:
         secs, cflops, desc = oracle_sample(w, tensors, args.ref_budget)
         cpu = {"value": cflops / secs / 1e12, "unit": UNIT, "cores": cpu_cores(),
                "kind": "oracle", "sample": desc}
@@ -433,7 +482,7 @@ def run_cuda(args, w):
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.describe(), "seed": w.seed, "flops_per_step": flops,
                    "l2": "flushed (256 MB write) before every timed step",
-                   "kernel": args.kernel,
+                   "kernel": args.kernel, "deterministic": bool(args.deterministic),
                    "pct_of_bf16_peak": 100.0 * value / peak},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak, "traffic": traffic,
@@ -463,11 +512,13 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7])
+    ap.add_argument("--workload", type=int, default=2, choices=list(range(1, 13)))
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tcgen05"])
     ap.add_argument("--ref-budget", type=float, default=10.0,
                     help="seconds of oracle work per timed sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="add the dQ partials in a fixed order (bitwise reproducible dQ)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)          # timing rule: at least 3 warm-up steps
     from varlen_flashattention_backward_gb300 import workloads as wl

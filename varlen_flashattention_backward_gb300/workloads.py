@@ -63,6 +63,10 @@ class Workload:
     mask_seed: int = 0x5EED
     n_heads_kv: int = 0           # 0 -> same as n_heads
     lens_kv: list = field(default=None)
+    sparse_mode: int = 0
+    q_start: list = field(default=None)    # outer split: per-sequence chunk starts
+    kv_start: list = field(default=None)
+    mask_density: float = 0.0     # > 0: an explicit attention mask, this share excluded
 
     def __post_init__(self):
         if not self.n_heads_kv:
@@ -100,6 +104,16 @@ class Workload:
              f"N={self.n_heads} D={self.head_dim} mask={mask}")
         if self.keep_prob < 1.0:
             s += f" dropout keep_prob={self.keep_prob}"
+        if self.lens_kv != self.lens:
+            s += f" lens_kv={_short(self.lens_kv)}"
+        if self.n_heads_kv != self.n_heads:
+            s += f" Nkv={self.n_heads_kv}"
+        if self.sparse_mode:
+            s += f" sparse_mode={self.sparse_mode}"
+        if self.q_start is not None:
+            s += f" q_start={_short(self.q_start)} kv_start={_short(self.kv_start)}"
+        if self.mask_density > 0:
+            s += f" atten_mask density={self.mask_density}"
         return s
 
 
@@ -132,6 +146,24 @@ def workload(cid: int, seed: int = 0) -> Workload:
     if cid == 7:
         # head dim 64: the bench mix with twice the heads (the same bytes)
         return Workload(7, "bf16", [512, 1024, 2048, 512], 32, 64, UNBOUNDED, 0, seed=seed)
+    bench_lens = [512, 1024, 2048, 512]
+    if cid == 8:
+        # grouped-query heads: 32 query heads on 8 key/value heads
+        return Workload(8, "bf16", bench_lens, 32, 128, UNBOUNDED, 0, seed=seed, n_heads_kv=8)
+    if cid == 9:
+        return Workload(9, "fp16", bench_lens, 16, 128, UNBOUNDED, 0, seed=seed)
+    if cid == 10:
+        # outer split: the second half of four causal 2048-token sequences
+        return Workload(10, "bf16", [1024] * 4, 16, 128, UNBOUNDED, 0, seed=seed,
+                        lens_kv=[2048] * 4, q_start=[1024] * 4, kv_start=[0] * 4)
+    if cid == 11:
+        # bottom-right causal (sparseMode 3): queries are the last part of the keys
+        return Workload(11, "bf16", [256, 512, 1024, 256], 16, 128, UNBOUNDED, 0, seed=seed,
+                        lens_kv=[1024, 2048, 4096, 1024], sparse_mode=3)
+    if cid == 12:
+        # an explicit mask (sparseMode 1), 30% of the pairs excluded
+        return Workload(12, "bf16", bench_lens, 16, 128, UNBOUNDED, UNBOUNDED, seed=seed,
+                        sparse_mode=1, mask_density=0.3)
     raise ValueError(f"unknown workload {cid}")
 
 
@@ -148,6 +180,16 @@ def make_tensors(w: Workload):
     dy = torch.randn(shp_q, generator=g, dtype=torch.float32) * w.dy_std
     dt = w.torch_dtype
     return q.to(dt), k.to(dt), v.to(dt), dy.to(dt)
+
+
+def make_atten_mask(w: Workload):
+    """The workload's explicit attention mask (uint8, 1 = excluded), drawn
+    from its seed, or None."""
+    if w.mask_density <= 0:
+        return None
+    g = np.random.default_rng(w.seed + 77)
+    rows, cols = max(w.lens), max(w.lens_kv)
+    return (g.random((rows, cols)) < w.mask_density).astype(np.uint8)
 
 
 def make_tensors_on_device(w: Workload, device):
