@@ -111,8 +111,8 @@ typedef struct {
   int32_t impl;            /* fa_bwd_impl */
   /* Nonzero: bitwise-reproducible dq.  Each CTA takes its work item from a
    * ticket counter in the workspace header, the items of one (sequence,
-   * head) unit run in ascending key-tile order, and the dq partial of every
-   * (query head, 64-row query tile) is added in ascending key-tile order,
+   * head) unit run in descending key-tile order, and the dq partial of every
+   * (query head, 64-row query tile) is added in descending key-tile order,
    * each adder waiting (bounded by wait_timeout_ns) on a per-tile counter
    * for the one before it.  A CTA waits only on items taken before its own,
    * so the waits always end.  dk and dv are deterministic in either mode.

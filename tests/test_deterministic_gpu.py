@@ -1,5 +1,5 @@
 """Deterministic mode: the dQ partials of each (query head, query tile) are
-added in ascending key-tile order, so repeated calls give the same dQ bit for
+added in descending key-tile order, so repeated calls give the same dQ bit for
 bit.  The result must still match the fp64 oracle to the usual tolerance."""
 
 import numpy as np

@@ -172,7 +172,7 @@ std::vector<SeqInfo> build_seqs(const Problem &pr) {
 // heads; unit order kept workloads of 0.4-1.1 GB 2-50% faster).
 // In unit order the last `tail_items` items (two waves of CTAs) are still
 // sorted longest first, so that no long item starts last (-5% on 8 x 2048
-// tokens x 16 heads).  `tile_order` keeps each unit's items in ascending
+// tokens x 16 heads).  `tile_order` keeps each unit's items in descending
 // key-tile order (the deterministic mode).  With `head_pairs` a unit is two
 // adjacent kv heads (the last may hold one): WorkItem::head is then
 // first | (count - 1) << 16.
@@ -209,6 +209,8 @@ std::vector<WorkItem> build_bwd_items(const Problem &pr, int kv_tile, bool tile_
                          [](const WorkItem &a, const WorkItem &c) {
                            return item_count(a) > item_count(c);
                          });
+      else   // deterministic mode: descending key tiles (see build_qtables)
+        std::reverse(items.begin() + u.first, items.end());
       if (tiles > 0) units.push_back(u);
     }
   }
@@ -294,13 +296,19 @@ void build_qtables(const Problem &pr, const std::vector<SeqInfo> &seqs,
       ++cnt[g0 + t];
     }
   }
+  // The first half holds, per query tile, the highest key tile that visits
+  // it: partials are added in descending key-tile order.  Each key tile
+  // walks its query tiles upward from its diagonal, so under a causal or
+  // banded window the next higher key tile reaches every query tile one
+  // or two tiles earlier, and the adds seldom wait (ascending order made
+  // every key tile wait for all lower ones at each query tile).
   tab.assign(2 * g_tiles, 0);
   *contiguous = true;
   for (size_t g = 0; g < g_tiles; ++g) {
     tab[g_tiles + g] = cnt[g];
     if (cnt[g] == 0) continue;
     if (hi[g] - lo[g] + 1 != cnt[g]) *contiguous = false;
-    tab[g] = lo[g];
+    tab[g] = hi[g];
   }
 }
 

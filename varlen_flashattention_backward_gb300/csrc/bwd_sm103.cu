@@ -642,9 +642,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tmem_ld32(tmem + lane_off + COL_DQ + 32, b);
       tc_fence_before();
       if (lane == 0) mbar_arrive(bar(B_DQFREE));
-      // Deterministic mode: wait until the key tiles before this one have
-      // added their partials of this query tile (the counter holds how many
-      // have), add, then publish count + 1.
+      // Deterministic mode: wait until the key tiles before this one in the add
+      // order (descending key tiles) have added their partials of this query tile
+      // (the counter holds how many have), add, then publish count + 1.
       int32_t *ctr = nullptr;
       int rank = 0;
       if constexpr (kDet) {

@@ -98,8 +98,10 @@ __device__ __forceinline__ int32_t *dq_counter(const BwdParams &p, const SeqInfo
                                                int qt) {
   return p.sem + int64_t(n) * (p.tp / kQTile) + s.qpad / kQTile + qt;
 }
+// Place of key tile `tile` in the add order of query tile qt (descending
+// key tiles: the table holds the highest one that visits qt).
 __device__ __forceinline__ int dq_rank(const BwdParams &p, const SeqInfo &s, int tile, int qt) {
-  return tile - p.qfirst[s.qpad / kQTile + qt];
+  return p.qfirst[s.qpad / kQTile + qt] - tile;
 }
 
 }  // namespace fav

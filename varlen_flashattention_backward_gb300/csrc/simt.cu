@@ -344,8 +344,8 @@ __global__ void __launch_bounds__(256) bwd_simt_kernel(BwdParams p) {
 #pragma unroll
           for (int c = 0; c < DC; ++c) dq[a][c] = fmaf(sv[a], kv[c], dq[a][c]);
       }
-      // Deterministic mode: add after the key tiles before this one, in
-      // ascending order, then let the next one in.
+      // Deterministic mode: add after the key tiles above this one (the
+      // order is descending), then let the next one in.
       int32_t *ctr = nullptr;
       int rank = 0;
       if (p.deterministic) {
