@@ -114,10 +114,16 @@ def test_sparse_modes_against_oracle(name, impl):
                  TOL[w.dtype])
 
 
-def _random_mask(w, seed, density):
-    """Seeded uint8 mask, a few rows / columns wider than the longest sequence."""
+def _random_mask(w, seed, density, pitch16=False):
+    """Seeded uint8 mask, a few rows / columns wider than the longest
+    sequence; with pitch16 its row pitch is a multiple of 16 bytes (the
+    tensor-core kernel then loads its tiles by TMA)."""
     g = np.random.default_rng(seed)
     rows, cols = max(w.lens) + 3, max(w.lens_kv) + 5
+    if pitch16:
+        cols = (cols + 15) // 16 * 16
+    elif cols % 16 == 0:
+        cols += 1
     return (g.random((rows, cols)) < density).astype(np.uint8)
 
 
@@ -135,13 +141,14 @@ MASK_CASES = {
 }
 
 
+@pytest.mark.parametrize("pitch16", [False, True])
 @pytest.mark.parametrize("impl", ["simt", "tcgen05"])
 @pytest.mark.parametrize("name", list(MASK_CASES))
-def test_atten_mask_against_oracle(name, impl):
+def test_atten_mask_against_oracle(name, impl, pitch16):
     w, mode, density = MASK_CASES[name]
     if impl == "tcgen05" and (w.dtype == "fp32" or w.head_dim not in (64, 128)):
         pytest.skip("tcgen05 kernel not built for this case")
-    am_np = _random_mask(w, w.seed, density)
+    am_np = _random_mask(w, w.seed, density, pitch16)
     am = torch.from_numpy(am_np).to(DEV)
     tensors = wl.make_tensors(w)
     mask_np = wl.make_keep_mask(w)

@@ -645,6 +645,7 @@ fa_status fa_varlen_bwd_ex(const void *q, const void *k, const void *v, const vo
                                                            : kDefaultTimeoutNs;
   p.atten_mask = pr.mask_used();
   p.am_cols = pr.am_cols;
+  p.am_rows = pr.am_rows;
 
   void *const *ev = options ? options->events : nullptr;
   auto mark = [&](int i) {

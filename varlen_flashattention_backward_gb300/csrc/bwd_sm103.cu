@@ -81,6 +81,13 @@ constexpr uint32_t SM_BAR = SM_DSUM + STAGES * 256;
 constexpr uint32_t SM_TOTAL = SM_BAR + 256;
 constexpr uint32_t SMEM_BYTES = SM_TOTAL + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+// With an explicit attention mask: STAGES x [64 queries x 128 keys] bytes of
+// it, loaded by TMA beside each Q/dY stage (only that instantiation asks
+// for the extra shared memory).
+constexpr uint32_t SM_AM = SM_TOTAL;
+constexpr uint32_t AM_STAGE = 64 * 128;
+constexpr uint32_t SMEM_BYTES_MASK = SM_AM + STAGES * AM_STAGE + 1024;
+static_assert(SMEM_BYTES_MASK <= 232448, "shared memory per CTA");
 
 // mbarrier slots
 enum : int {
@@ -98,6 +105,7 @@ enum : int {
 struct TcMaps {
   CUtensorMap q, dy, k, v;
   CUtensorMap dk, dv;   // same shape as k / v, for the epilogue's bulk stores
+  CUtensorMap am;       // the explicit mask, when it is loaded by TMA
 };
 
 // Bits [bit, bit + 32) of the keep mask, read without leaving
@@ -311,7 +319,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int qy = sq.cu_q + q0, qx = n * DD;
         const uint32_t full = bar(B_FULL + st);
         const int64_t srow = int64_t(n) * p.tp + sq.qpad + q0;
-        mbar_arrive_expect_tx_w(full, 2 * NBOX * 8192 + 2 * 256);
+        const bool am_tile = kMask && p.am_tma;
+        mbar_arrive_expect_tx_w(full, 2 * NBOX * 8192 + 2 * 256 + (am_tile ? AM_STAGE : 0u));
+        if (am_tile)   // mask rows q0.., columns k0.. (chunk-local); out of range reads 0
+          tma_load_2d_w(sb + SM_AM + st * AM_STAGE, &maps.am, full, k0, q0);
         for (int bx = 0; bx < NBOX; ++bx) {
           tma_load_2d_w(sb + SM_Q + st * 16384 + bx * 8192, &maps.q, full, qx + 64 * bx, qy);
           tma_load_2d_w(sb + SM_DY + st * 16384 + bx * 8192, &maps.dy, full, qx + 64 * bx, qy);
@@ -466,12 +477,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
       if (kMask && jg < sq.len_k) {
-        // Explicit mask: for each of its 32 queries a warp reads 32
-        // consecutive bytes (its 32 keys) of one mask row.
+        if (p.am_tma) {
+          // the stage's mask tile: row = query - q0, column = key - k0
+          const uint8_t *am = sm + SM_AM + st * AM_STAGE + (32 * half) * 128 + jl;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int i = i0 + c;
-          if (i < sq.len_q && atten_masked(p.atten_mask, p.am_cols, i, jg)) pr[c] = 0.f;
+          for (int c = 0; c < 32; ++c)
+            if (i0 + c < sq.len_q && am[c * 128] != 0) pr[c] = 0.f;
+        } else {
+          // Explicit mask from global memory: for each of its 32 queries a
+          // warp reads 32 consecutive bytes (its 32 keys) of one mask row.
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int i = i0 + c;
+            if (i < sq.len_q && atten_masked(p.atten_mask, p.am_cols, i, jg)) pr[c] = 0.f;
+          }
         }
       }
       uint32_t keep = 0xFFFFFFFFu;
@@ -772,7 +791,7 @@ bool make_map(CUtensorMap *m, const void *base, int64_t rows, int heads, int d, 
 template <bool kBF16, bool kDet, bool kMask, bool kD64>
 cudaError_t launch_t(const BwdParams &p, cudaStream_t st) {
   const int d = kD64 ? 64 : HD;
-  TcMaps maps;
+  TcMaps maps{};
   if (!make_map(&maps.q, p.q, p.total_q, p.n, d, BM, kBF16) ||
       !make_map(&maps.dy, p.dy, p.total_q, p.n, d, BM, kBF16) ||
       !make_map(&maps.k, p.k, p.total_kv, p.n_kv, d, BN, kBF16) ||
@@ -780,16 +799,36 @@ cudaError_t launch_t(const BwdParams &p, cudaStream_t st) {
       !make_map(&maps.dk, p.dk, p.total_kv, p.n_kv, d, BN, kBF16) ||
       !make_map(&maps.dv, p.dv, p.total_kv, p.n_kv, d, BN, kBF16))
     return cudaErrorInvalidValue;
+  BwdParams q = p;
+  q.am_tma = 0;
+  if (kMask) {
+    // TMA needs a 16-byte aligned base and row pitch; otherwise the softmax
+    // warps read the mask from global memory.
+    const bool al = (reinterpret_cast<uintptr_t>(p.atten_mask) & 15u) == 0 && p.am_cols % 16 == 0;
+    if (al) {
+      EncodeTiledFn enc = encode_fn();
+      if (enc == nullptr) return cudaErrorInvalidValue;
+      cuuint64_t dims[2] = {cuuint64_t(p.am_cols), cuuint64_t(p.am_rows)};
+      cuuint64_t strides[1] = {cuuint64_t(p.am_cols)};
+      cuuint32_t box[2] = {128, 64};
+      cuuint32_t es[2] = {1, 1};
+      if (enc(&maps.am, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(p.atten_mask),
+              dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+      q.am_tma = 1;
+    }
+  }
+  const uint32_t smem = kMask ? SMEM_BYTES_MASK : SMEM_BYTES;
   cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<kBF16, kDet, kMask, kD64>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   int dev = 0;
-  BwdParams q = p;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&q.prefetch_ahead, cudaDevAttrMultiProcessorCount, dev)) !=
       cudaSuccess)
     return e;
-  bwd_tc_kernel<kBF16, kDet, kMask, kD64><<<p.n_items, NTHREADS, SMEM_BYTES, st>>>(q, maps);
+  bwd_tc_kernel<kBF16, kDet, kMask, kD64><<<p.n_items, NTHREADS, smem, st>>>(q, maps);
   return cudaGetLastError();
 }
 

@@ -81,10 +81,12 @@ struct BwdParams {
   float scale, scale_log2, inv_keep;
   int use_dropout;
   long long timeout_ns;
-  // Explicit attention mask (uint8 [rows][am_cols], 1 = excluded) at each
-  // sequence's chunk-local (i, j), or null.
+  // Explicit attention mask (uint8 [am_rows][am_cols], 1 = excluded) at
+  // each sequence's chunk-local (i, j), or null.
   const uint8_t *atten_mask;
   int64_t am_cols;
+  int64_t am_rows;
+  int am_tma;   // tcgen05 kernel: the mask tiles come in by TMA (set at launch)
 };
 
 struct FwdParams {
