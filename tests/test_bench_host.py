@@ -17,6 +17,27 @@ import bench  # noqa: E402
 from varlen_flashattention_backward_gb300 import workloads as wl  # noqa: E402
 
 
+@pytest.mark.parametrize("cid", [10, 11, 12])
+def test_feature_workload_pairs_match_the_oracle_window(cid):
+    """The FLOP count of the feature workloads (outer split, bottom-right
+    causal, explicit mask) against a brute-force count over the oracle's
+    window and mask of every sequence."""
+    import numpy as np
+    import oracle
+    w = wl.workload(cid)
+    am = wl.make_atten_mask(w)
+    want = 0
+    for b, (lq, lk) in enumerate(zip(w.lens, w.lens_kv)):
+        pre, nxt = oracle.mode_window(w.sparse_mode, w.pre_tokens, w.next_tokens, lq, lk)
+        qs = w.q_start[b] if w.q_start else 0
+        ks = w.kv_start[b] if w.kv_start else 0
+        ok = oracle.window_allowed(lq, lk, pre, nxt, q_start=qs, kv_start=ks)
+        if am is not None and w.sparse_mode in (0, 1, 4):
+            ok &= am[:lq, :lk] == 0
+        want += int(ok.sum())
+    assert bench.workload_pairs(w, am) == want
+
+
 def test_flop_count_matches_closed_forms():
     # causal: L (L + 1) / 2 pairs per head
     w2 = wl.workload(2)
