@@ -251,15 +251,21 @@ fa_status fa_varlen_bwd_ex(
  *     64 MiB are rejected with FA_ERR_WORKSPACE before any launch.  Example:
  *     the fp32 dQ accumulator alone takes total_q * head_num * head_dim * 4
  *     bytes.
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture on the device.
- *   - Every call on a device shares the one array and leaves its contents
+ *   - The array exists once per CUDA context: in the device's primary
+ *     context (the one the runtime and PyTorch use) and in any other
+ *     context, made through the driver API, that calls this entry point.
+ *   - The first call in a context looks up the array's device address
+ *     there (cudaGetSymbolAddress, with that context current) and caches
+ *     it under the context's unique id; make that first call before any
+ *     stream capture in the context.  cudaDeviceReset destroys the primary
+ *     context and the array with it; the next call, in the new primary
+ *     context, looks the address up again.
+ *   - Every call in a context shares the one array and leaves its contents
  *     behind; each call re-initialises what it needs.  Calls whose GPU work
  *     overlaps (other streams, other host threads) race on the array and
  *     give wrong results: serialise them.
- *   - The error word it uses is internal; fa_varlen_read_error cannot read
- *     it. */
+ *   - A bounded in-kernel wait that expires leaves its code in the array's
+ *     error word; fa_varlen_bwd_static_scratch_read_error reads it. */
 fa_status fa_varlen_bwd_static_scratch(
     const void *q, const void *k, const void *v, const void *dy,
     const uint8_t *drop_mask, int64_t drop_mask_bytes,
@@ -270,6 +276,14 @@ fa_status fa_varlen_bwd_static_scratch(
     double keep_prob, int64_t pre_tokens, int64_t next_tokens,
     int64_t sparse_mode,
     void *dq, void *dk, void *dv, fa_stream_t stream);
+
+/* The error word of the last fa_varlen_bwd_static_scratch call in the
+ * current context, read after synchronising `stream` (the stream that call
+ * ran on): FA_OK, or FA_ERR_TIMEOUT when a bounded in-kernel wait expired
+ * and that call's dq / dk / dv are invalid.  *code receives the raw word
+ * (0 = no error).  It allocates nothing.  Errors: FA_ERR_NULLPTR (code),
+ * FA_ERR_CUDA. */
+fa_status fa_varlen_bwd_static_scratch_read_error(fa_stream_t stream, int32_t *code);
 
 /* Reads the error word that the last call on `workspace` left in it, after
  * synchronising `stream`: FA_OK, or FA_ERR_TIMEOUT when a bounded in-kernel

@@ -76,6 +76,7 @@ _SIGS = {
     "fa_varlen_bwd_static_scratch": ([_vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp] +
                                      _SCALARS[:8] + [_i32, _cp, _f64, _f64, _i64, _i64, _i64,
                                                      _vp, _vp, _vp, _vp], _i32),
+    "fa_varlen_bwd_static_scratch_read_error": ([_vp, ctypes.POINTER(ctypes.c_int32)], _i32),
     "fa_varlen_selftest_wait_timeout": ([_vp, _sz, _i64, _vp], _i32),
     "fa_varlen_bwd_schedule": ([_pi64, _pi64, _i64, _i64, _i64, _i64, _i32,
                                 ctypes.POINTER(ctypes.c_int32), _i64, _pi64], _i32),
@@ -290,6 +291,17 @@ def bwd_static_scratch(q, k, v, dy, y, softmax_max, softmax_sum, lens_q, lens_kv
         b"TND", float(scale), float(keep_prob), int(pre_tokens), int(next_tokens), 0, _ptr(dq),
         _ptr(dk), _ptr(dv), _stream(stream)), "fa_varlen_bwd_static_scratch")
     return dq, dk, dv
+
+
+def static_scratch_read_error(stream=None) -> int:
+    """Raw error word of the last fa_varlen_bwd_static_scratch call in the
+    current context (fa_varlen_bwd_static_scratch_read_error; synchronises
+    `stream`)."""
+    code = ctypes.c_int32(0)
+    st = lib().fa_varlen_bwd_static_scratch_read_error(_stream(stream), ctypes.byref(code))
+    if st not in (FA_OK, FA_ERR_TIMEOUT):
+        _check(st, "fa_varlen_bwd_static_scratch_read_error")
+    return int(code.value)
 
 
 def selftest_wait_timeout(workspace, wait_timeout_ns, stream=None):

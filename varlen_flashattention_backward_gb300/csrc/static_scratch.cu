@@ -7,9 +7,10 @@
 // or a host thread that must not take the allocator's locks.  This entry
 // point takes no workspace.  Its scratch (the work list, the padded
 // statistics, the fp32 dQ accumulator and the error word) lives in the
-// file-scope array below, which the CUDA module reserves on every device
-// that loads this library and keeps until the process exits.
+// file-scope array below, which the CUDA module reserves in every context
+// that loads this library and keeps until that context is destroyed.
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <array>
@@ -20,27 +21,93 @@
 namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(64) << 20;   // 64 MiB
-constexpr int kMaxDevices = 64;
+constexpr int kMaxContexts = 64;
 
 // The scratch itself.  In host code this name is only a host-side stand-in;
 // the device address comes from cudaGetSymbolAddress.
 __device__ __align__(256) unsigned char g_bwd_scratch[kStaticScratchBytes];
 
-std::mutex g_mu;
-std::array<void *, kMaxDevices> g_ptr{};   // device address per device, once known
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
 
-// Device address of g_bwd_scratch on the current device, looked up once per
-// device (with that device current) and cached.  Null on failure.
-void *scratch_address() {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_ptr[dev] == nullptr) {
-    void *ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_bwd_scratch) != cudaSuccess) return nullptr;
-    g_ptr[dev] = ptr;
+struct DriverFns {
+  CtxGetCurrentFn get_current = nullptr;
+  CtxGetIdFn get_id = nullptr;
+};
+
+const DriverFns &driver_fns() {
+  static DriverFns fns;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fns.get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fns.get_id = reinterpret_cast<CtxGetIdFn>(p);
+    cudaGetLastError();
+  });
+  return fns;
+}
+
+// Address of g_bwd_scratch, one entry per CUDA context.  The key is the
+// context's unique id (cuCtxGetId), which the driver never gives to another
+// context of the process: a context that is destroyed and created again
+// (cudaDeviceReset, then the next runtime call) or a second context on the
+// same device (created through the driver API) gets a lookup of its own.
+struct Entry {
+  unsigned long long ctx_id;
+  void *ptr;
+};
+std::mutex g_mu;
+std::array<Entry, kMaxContexts> g_table{};
+int g_used = 0;
+
+// Unique id of the context current on this thread; the device's primary
+// context is made current first when none is.  0 on failure.
+unsigned long long current_context_id() {
+  const DriverFns &f = driver_fns();
+  if (f.get_current == nullptr || f.get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  if (f.get_current(&ctx) != CUDA_SUCCESS) return 0;
+  if (ctx == nullptr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    if (f.get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
   }
-  return g_ptr[dev];
+  unsigned long long id = 0;
+  if (f.get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of g_bwd_scratch in the current context: looked up once
+// per context (cudaGetSymbolAddress with that context current; the first
+// lookup also loads this library's module into the context) and cached.
+// Null on failure, with the runtime's last-error state cleared.
+void *scratch_address() {
+  const unsigned long long id = current_context_id();
+  if (id == 0) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (int i = 0; i < g_used; ++i)
+    if (g_table[i].ctx_id == id) return g_table[i].ptr;
+  void *ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_bwd_scratch) != cudaSuccess || ptr == nullptr) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  // A full table (more than kMaxContexts contexts over the process's life)
+  // recycles the oldest entry.
+  const int slot = g_used < kMaxContexts ? g_used++ : int(id % kMaxContexts);
+  g_table[slot] = Entry{id, ptr};
+  return ptr;
 }
 
 }  // namespace
@@ -65,4 +132,12 @@ extern "C" fa_status fa_varlen_bwd_static_scratch(
                        seq_lens_q, seq_lens_kv, batch, total_q, total_kv, head_num, head_num_kv,
                        head_dim, dtype, layout, scale, keep_prob, pre_tokens, next_tokens,
                        sparse_mode, dq, dk, dv, scratch, kStaticScratchBytes, stream);
+}
+
+extern "C" fa_status fa_varlen_bwd_static_scratch_read_error(fa_stream_t stream,
+                                                             int32_t *code) {
+  if (code == nullptr) return FA_ERR_NULLPTR;
+  void *scratch = scratch_address();
+  if (scratch == nullptr) return FA_ERR_CUDA;
+  return fa_varlen_read_error(scratch, kStaticScratchBytes, stream, code);
 }
