@@ -36,6 +36,16 @@ def device_mask(w: wl.Workload, dev):
     return fa.gen_keep_mask(w.mask_bits, w.mask_seed, w.keep_prob, device=dev)
 
 
+def nan_workspace(w: wl.Workload, dev, impl=fa.FA_BWD_AUTO):
+    """A backward workspace whose every byte is 0xFF (every fp32 word a NaN),
+    so that any scratch the backward reads before writing poisons its
+    outputs."""
+    nbytes = fa.bwd_workspace_size(w.lens, w.lens_kv, w.n_heads, w.n_heads_kv, w.head_dim,
+                                   w.torch_dtype, w.keep_prob, w.pre_tokens, w.next_tokens,
+                                   impl)
+    return torch.full((nbytes,), 255, dtype=torch.uint8, device=dev)
+
+
 def gpu_forward_backward(w: wl.Workload, tensors, dev, impl=fa.FA_BWD_AUTO, mask=None,
                          q_start=None, kv_start=None):
     q, k, v, dy = (t.to(dev) for t in tensors)
@@ -43,7 +53,7 @@ def gpu_forward_backward(w: wl.Workload, tensors, dev, impl=fa.FA_BWD_AUTO, mask
                            w.keep_prob, mask, q_start=q_start, kv_start=kv_start)
     dq, dk, dv = fa.bwd(q, k, v, dy, y, smax, ssum, w.lens, w.lens_kv, w.scale, w.pre_tokens,
                         w.next_tokens, w.keep_prob, mask, impl=impl, q_start=q_start,
-                        kv_start=kv_start)
+                        kv_start=kv_start, workspace=nan_workspace(w, dev, impl))
     torch.cuda.synchronize()
     return dict(y=y, smax=smax, ssum=ssum, dq=dq, dk=dk, dv=dv)
 

@@ -72,6 +72,19 @@ SMALL = {
     "fp16_causal": wl.Workload(13, "fp16", [100, 33], 2, 128, BIG, 0, seed=6),
     "lq_ne_lk": wl.Workload(14, "bf16", [50, 90], 2, 128, 30, 10, seed=7, lens_kv=[120, 40]),
     "fp32_dropout_band": wl.Workload(15, "fp32", [70, 45], 2, 128, 20, 3, keep_prob=0.7, seed=8),
+    # Key lengths that are multiples of 128: the tensor-core kernel copies
+    # the keep bits of each stage into shared memory (ragged query lengths,
+    # an empty sequence, grouped heads, Lq != Lk).
+    "dropout_rows16_gqa": wl.Workload(24, "bf16", [256, 0, 384, 128], 4, 128, 100, 20,
+                                      keep_prob=0.8, seed=17, n_heads_kv=2),
+    "dropout_rows16_lq_ne_lk": wl.Workload(25, "bf16", [200, 50, 131], 2, 128, BIG, 40,
+                                           keep_prob=0.9, seed=18, lens_kv=[256, 128, 384]),
+    "d64_dropout_rows16": wl.Workload(26, "bf16", [256, 77, 128], 3, 64, 90, 0, keep_prob=0.85,
+                                      seed=19, lens_kv=[256, 128, 128]),
+    # No key reaches query rows 0-129 (nextTokens = -130): query tiles 0 and
+    # 1 have no key tile at all, so their dQ rows come only from the
+    # accumulator rows the preprocess zeroes.
+    "unvisited_query_tiles": wl.Workload(27, "bf16", [300, 200], 2, 128, BIG, -130, seed=20),
 }
 
 
@@ -197,31 +210,57 @@ def _full_size_run(cid):
     return w, tensors, out
 
 
-def _invariants(w, out):
-    """Over every (sequence, head): sum_j dK_j = 0 (each dS row sums to 0),
-    and nothing is non-finite."""
-    cq, ck = oracle.cu_seqlens(w.lens), oracle.cu_seqlens(w.lens_kv)
+def _invariants(w, tensors, out):
+    """Identities of the exact backward, checked on every (sequence, kv head)
+    unit of a full-size run, each against the size of its own terms (bound
+    tol * sum of |terms|, tol the parity tolerance):
+    - sum_j dK_j = 0 for every column d (each dS row sums to 0);
+    - sum dQ o Q over the unit's query heads = sum dK o K (both equal
+      sum_ij dS_ij S_ij);
+    - sum dV o V = sum dY o Y over the unit's query heads (Y = P V).
+    A unit with a wrong or missing key tile, or with dQ rows of another
+    unit, breaks at least one of them; nothing may be non-finite."""
     for name in ("dq", "dk", "dv", "y"):
         assert torch.isfinite(out[name]).all(), name
-    dk = out["dk"].double()
+    tol = TOL[w.dtype]
+    cq, ck = oracle.cu_seqlens(w.lens), oracle.cu_seqlens(w.lens_kv)
+    group = w.n_heads // w.n_heads_kv
+    dev = out["dk"].device
+    q, k, v, dy = (t.to(dev) for t in tensors)
     for b in range(len(w.lens)):
-        seg = dk[ck[b]:ck[b + 1]]
-        s = seg.sum(dim=0).abs().max().item()
-        a = seg.abs().sum(dim=0).max().item()
-        assert s <= 2e-2 * a, (b, s, a)
+        qs, ks = slice(cq[b], cq[b + 1]), slice(ck[b], ck[b + 1])
+        if cq[b + 1] == cq[b] or ck[b + 1] == ck[b]:
+            continue
+        for h in range(w.n_heads_kv):
+            hs = slice(h * group, (h + 1) * group)
+            dk = out["dk"][ks, h].double()
+            kk = k[ks, h].double()
+            s = dk.sum(dim=0).abs()
+            a = dk.abs().sum(dim=0)
+            assert bool((s <= tol * a + 1e-30).all()), (b, h, float(s.max()), float(a.max()))
+            qq = q[qs, hs].double()
+            dq = out["dq"][qs, hs].double()
+            lhs, rhs = (dq * qq).sum(), (dk * kk).sum()
+            bound = tol * ((dq * qq).abs().sum() + (dk * kk).abs().sum())
+            assert abs(float(lhs - rhs)) <= float(bound), (b, h, float(lhs), float(rhs))
+            dv, vv = out["dv"][ks, h].double(), v[ks, h].double()
+            yy, dyy = out["y"][qs, hs].double(), dy[qs, hs].double()
+            lhs, rhs = (dv * vv).sum(), (dyy * yy).sum()
+            bound = tol * ((dv * vv).abs().sum() + (dyy * yy).abs().sum())
+            assert abs(float(lhs - rhs)) <= float(bound), (b, h, float(lhs), float(rhs))
 
 
 @pytest.mark.parametrize("cid,units", [
-    (3, "longest2+shortest1"),
-    (4, [(1, 7)]),
-    (5, [(1, 3)]),
+    (3, "longest2+shortest2"),
+    (4, [(0, 0), (0, 7), (1, 0), (1, 7)]),
+    (5, [(0, 0), (0, 15), (3, 0), (3, 15)]),
 ])
 def test_full_size_sampled_units(cid, units):
     w, tensors, out = _full_size_run(cid)
-    _invariants(w, out)
-    if units == "longest2+shortest1":
+    _invariants(w, tensors, out)
+    if units == "longest2+shortest2":
         lo, hi = int(np.argmin(w.lens)), int(np.argmax(w.lens))
-        units = [(hi, 0), (hi, w.n_heads - 1), (lo, 5)]
+        units = [(hi, 0), (hi, w.n_heads - 1), (lo, 5), (lo, w.n_heads - 1)]
     for b, n in units:
         errs = unit_check(w, tensors, out, b, n)
         tol = TOL[w.dtype]

@@ -365,25 +365,34 @@ constexpr size_t kPageableCopyPiece = size_t(64) << 10;
 
 // Uploads [header | seqs | items | table]; the header's error word and
 // ticket are 0.
+// Copies host bytes to the device in pageable pieces of at most
+// kPageableCopyPiece bytes.
+fa_status copy_pieces(uint8_t *dst, const uint8_t *src, size_t bytes, cudaStream_t st) {
+  for (size_t off = 0; off < bytes; off += kPageableCopyPiece) {
+    const size_t n = std::min(kPageableCopyPiece, bytes - off);
+    if (cudaMemcpyAsync(dst + off, src + off, n, cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
+// Uploads [header (zeroed) | sequences | work list] and, when given, the
+// query-tile table at table_off (a separate copy: the work-list area is
+// sized for the finer tiling and mostly unused by the coarser one).
 fa_status upload_plan(void *ws, size_t seqs_off, size_t items_off,
                       const std::vector<SeqInfo> &seqs, const std::vector<WorkItem> &items,
                       cudaStream_t st, size_t table_off = 0,
                       const std::vector<int32_t> *table = nullptr) {
-  size_t bytes = items_off + sizeof(WorkItem) * items.size();
-  if (table && !table->empty()) bytes = table_off + sizeof(int32_t) * table->size();
+  const size_t bytes = items_off + sizeof(WorkItem) * items.size();
   std::vector<uint8_t> host(bytes, 0);
   std::memcpy(host.data() + seqs_off, seqs.data(), sizeof(SeqInfo) * seqs.size());
   if (!items.empty())
     std::memcpy(host.data() + items_off, items.data(), sizeof(WorkItem) * items.size());
-  if (table && !table->empty())
-    std::memcpy(host.data() + table_off, table->data(), sizeof(int32_t) * table->size());
-  for (size_t off = 0; off < bytes; off += kPageableCopyPiece) {
-    const size_t n = std::min(kPageableCopyPiece, bytes - off);
-    if (cudaMemcpyAsync(static_cast<uint8_t *>(ws) + off, host.data() + off, n,
-                        cudaMemcpyHostToDevice, st) != cudaSuccess)
-      return FA_ERR_CUDA;
-  }
-  return FA_OK;
+  uint8_t *dst = static_cast<uint8_t *>(ws);
+  fa_status r = copy_pieces(dst, host.data(), bytes, st);
+  if (r != FA_OK || table == nullptr || table->empty()) return r;
+  return copy_pieces(dst + table_off, reinterpret_cast<const uint8_t *>(table->data()),
+                     sizeof(int32_t) * table->size(), st);
 }
 
 uint64_t keep_threshold(double keep_prob, int *keep_all) {
@@ -609,13 +618,14 @@ fa_status fa_varlen_bwd_ex(const void *q, const void *k, const void *v, const vo
   const bool pairs = impl == FA_BWD_TCGEN05 && head_dim == 64 && !det;
   auto items = build_bwd_items(pr, tile, det, device_attr(cudaDevAttrL2CacheSize), pairs,
                                2 * device_attr(cudaDevAttrMultiProcessorCount));
+  // The deterministic mode's add order of each query tile.
   std::vector<int32_t> qtab;
   if (det) {
     bool contiguous = true;
     build_qtables(pr, seqs, items, qtab, &contiguous);
     if (!contiguous) return FA_ERR_UNSUPPORTED;
   }
-  st = upload_plan(workspace, L.seqs, L.items, seqs, items, cs, L.qfirst, det ? &qtab : nullptr);
+  st = upload_plan(workspace, L.seqs, L.items, seqs, items, cs, L.qfirst, &qtab);
   if (st != FA_OK) return st;
 
   uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -634,6 +644,12 @@ fa_status fa_varlen_bwd_ex(const void *q, const void *k, const void *v, const vo
   p.ticket = reinterpret_cast<int32_t *>(ws + kTicketOffset);
   p.sem = reinterpret_cast<int32_t *>(ws + L.sem);
   p.qfirst = reinterpret_cast<const int32_t *>(ws + L.qfirst);
+  // Dropout keep bits by 16-byte copies: every key tile of every mask row
+  // starts on a 16-byte boundary when all key lengths are multiples of 128
+  // (then so are the per-sequence bit offsets) and the mask is aligned.
+  p.drop_rows16 = dropout && (reinterpret_cast<uintptr_t>(drop_mask) & 15u) == 0;
+  for (int64_t b = 0; b < batch && p.drop_rows16; ++b)
+    if (seq_lens_kv[b] % kTcKvTile != 0) p.drop_rows16 = 0;
   p.n_items = int(items.size());
   p.batch = int(batch); p.n = int(head_num); p.n_kv = int(head_num_kv); p.d = int(head_dim);
   p.tp = int(pr.tp); p.total_q = int(total_q); p.total_kv = int(total_kv);
@@ -653,10 +669,6 @@ fa_status fa_varlen_bwd_ex(const void *q, const void *k, const void *v, const vo
            cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), cs) == cudaSuccess;
   };
   if (!mark(0)) return FA_ERR_CUDA;
-  if (det && pr.tp > 0 &&
-      cudaMemsetAsync(p.sem, 0, sizeof(int32_t) * size_t(pr.n * (pr.tp / kQTile)), cs) !=
-          cudaSuccess)
-    return FA_ERR_CUDA;
   if (pr.tp > 0 && launch_bwd_preprocess(p, dtype, cs) != cudaSuccess) return FA_ERR_CUDA;
   if (!mark(1)) return FA_ERR_CUDA;
   if (!items.empty()) {

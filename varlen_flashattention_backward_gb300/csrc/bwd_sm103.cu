@@ -78,16 +78,21 @@ constexpr uint32_t SM_DS = SM_DY + STAGES * 16384;    // [128 keys x 64 queries]
 constexpr uint32_t SM_LSE = SM_DS + 16384;            // STAGES x 64 floats
 constexpr uint32_t SM_DSUM = SM_LSE + STAGES * 256;
 constexpr uint32_t SM_BAR = SM_DSUM + STAGES * 256;
-constexpr uint32_t SM_TOTAL = SM_BAR + 256;
-constexpr uint32_t SMEM_BYTES = SM_TOTAL + 1024;
-static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+// The dropout instantiations keep each stage's keep bits after the
+// barriers when they come in by 16-byte copies (BwdParams::drop_rows16):
+// 64 query rows x 128 keys, one 16-byte chunk per row, LSB first.  Other
+// instantiations have no such area.
+constexpr uint32_t SM_DROP = SM_BAR + 256;
+constexpr uint32_t DROP_STAGE = 64 * 16;
+__host__ __device__ constexpr uint32_t sm_end(bool drop) { return SM_DROP + (drop ? STAGES * DROP_STAGE : 0u); }
+__host__ __device__ constexpr uint32_t smem_bytes(bool drop) { return sm_end(drop) + 1024; }
+static_assert(smem_bytes(true) <= 232448, "shared memory per CTA");
 // With an explicit attention mask: STAGES x [64 queries x 128 keys] bytes of
 // it, loaded by TMA beside each Q/dY stage (only that instantiation asks
 // for the extra shared memory).
-constexpr uint32_t SM_AM = SM_TOTAL;
 constexpr uint32_t AM_STAGE = 64 * 128;
-constexpr uint32_t SMEM_BYTES_MASK = SM_AM + STAGES * AM_STAGE + 1024;
-static_assert(SMEM_BYTES_MASK <= 232448, "shared memory per CTA");
+__host__ __device__ constexpr uint32_t smem_bytes_mask(bool drop) { return sm_end(drop) + STAGES * AM_STAGE + 1024; }
+static_assert(smem_bytes_mask(true) <= 232448, "shared memory per CTA");
 
 // mbarrier slots
 enum : int {
@@ -172,6 +177,52 @@ __device__ __forceinline__ void st_global_v4(void *ptr, uint32_t a, uint32_t b, 
                : "memory");
 }
 
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+// 16-byte asynchronous copy global -> shared (L2 only) by this thread.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src))
+               : "memory");
+}
+
+// Makes `bar` wait for this thread's cp.async copies issued so far: the
+// barrier's pending count goes up by one now and down by one when they
+// complete, so it must be called before the arrival that would complete the
+// phase.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Keep bits of one stage (BwdParams::drop_rows16): rows q0 .. q0 + rows - 1
+// of query head n, keys k0 .. k0 + 127, one 16-byte chunk per row (its bit
+// index mask_off + (n Lq + i) Lk + k0 is a multiple of 128), two rows per
+// lane, copied with cp.async and tracked by the stage barrier `full`.  The
+// whole producer warp calls it before the stage's arrive.expect_tx.
+__device__ __forceinline__ void load_keep_bits(uint32_t dst, const uint8_t *mask,
+                                               const SeqInfo &sq, int n, int q0, int k0,
+                                               int rows, uint32_t full, int lane) {
+  const int64_t bit0 = sq.mask_off + (int64_t(n) * sq.len_q + q0) * sq.len_k + k0;
+  for (int r = lane; r < rows; r += 32)
+    cp_async_16(dst + r * 16, mask + ((bit0 + int64_t(r) * sq.len_k) >> 3));
+  cp_async_mbar_arrive(full);
+  __syncwarp();
+}
+
+// Adds the dQ partial of one drain thread into dq_acc: its 16 four-column
+// segments (query rows 4j + c of the tile, c = lane % 4), rows < `rows`.
+__device__ __forceinline__ void dq_add(float *ptr, int64_t row_stride, const float (&out)[64],
+                                       int c, int rows) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j, ptr += 4 * row_stride)
+    if (4 * j + c < rows)
+      red_add_v4_f32(ptr, out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
+}
+
 // Named barrier 1 joins the four dQ drain warps (warps 12-15).
 __device__ __forceinline__ void drain_bar_sync() {
   asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -205,10 +256,11 @@ __device__ __forceinline__ bool wait_or_abort(const Ctl &c, uint32_t bar, uint32
 // load one box; S^T and dP^T take 4 k-steps and dV, dK are N = 64
 // products.  dQ^T keeps M = 128 (d) starting at the item's own K box, so
 // its rows 64-127 (the other box, or zeros) are not reduced.
-template <bool kBF16, bool kDet, bool kMask, bool kD64>
+template <bool kBF16, bool kDet, bool kMask, bool kD64, bool kDrop>
 __global__ void __launch_bounds__(NTHREADS, 1)
     bwd_tc_kernel(const BwdParams p, const __grid_constant__ TcMaps maps) {
   constexpr int DD = kD64 ? 64 : HD;   // head dim of the tensors
+  constexpr uint32_t SM_AM = sm_end(kDrop);   // explicit-mask stages
   constexpr int NBOX = DD / 64;         // 64-column boxes per row
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -279,6 +331,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int per_head = qcnt * group;   // iterations per kv head
   const int n_it = per_head * nh;
 
+  // Registers by warpgroup (setmaxnreg): the producer / MMA-issuer group
+  // gives up registers it does not use to the two softmax groups, whose
+  // 32-column S, dP and P rows are the kernel's largest live set; the drain
+  // group keeps the launch's 128.  The split stays within the 512 x 128
+  // registers the block was launched with: 4 warps x 32 x 72 + 8 x 32 x 152
+  // + 4 x 32 x 128 = 64512.
+  if (warp < 4) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // The whole warp runs this loop; copies are issued by one elected lane.
@@ -320,6 +380,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t full = bar(B_FULL + st);
         const int64_t srow = int64_t(n) * p.tp + sq.qpad + q0;
         const bool am_tile = kMask && p.am_tma;
+        const bool drop_tile = kDrop && p.drop_rows16;
+        const int rows = min(BM, sq.len_q - q0);
+        if (drop_tile)
+          load_keep_bits(sb + SM_DROP + st * DROP_STAGE, p.mask, sq, n, q0, k0, rows, full,
+                         lane);
         mbar_arrive_expect_tx_w(full, 2 * NBOX * 8192 + 2 * 256 + (am_tile ? AM_STAGE : 0u));
         if (am_tile)   // mask rows q0.., columns k0.. (chunk-local); out of range reads 0
           tma_load_2d_w(sb + SM_AM + st * AM_STAGE, &maps.am, full, k0, q0);
@@ -431,7 +496,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_wait(bar(B_FINAL), 0, drain_ns, &never);
       }
     }
-  } else if (warp >= 4 && warp < 12) {
+  }
+  } else if (warp < 12) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 152;");
     // ------------------------------------------------------------ softmax / dS
     const int half = (warp - 4) >> 2;
     const int quarter = warp & 3;
@@ -495,23 +562,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       uint32_t keep = 0xFFFFFFFFu;
       float zs = 1.f;
-      if (p.use_dropout) {
+      if constexpr (kDrop) {
         const int il = i0 + lane;
         uint32_t w = 0;
         if (il < sq.len_q) {
-          const int64_t bit = sq.mask_off + (int64_t(n) * sq.len_q + il) * sq.len_k + k0 +
-                              quarter * 32;
-          w = fetch_bits32(p.mask, p.mask_bytes, bit);
+          if (p.drop_rows16) {
+            w = ld_shared_u32(sb + SM_DROP + st * DROP_STAGE + (32 * half + lane) * 16 +
+                              quarter * 4);
+          } else {
+            const int64_t bit = sq.mask_off + (int64_t(n) * sq.len_q + il) * sq.len_k + k0 +
+                                quarter * 32;
+            w = fetch_bits32(p.mask, p.mask_bytes, bit);
+          }
         }
         keep = transpose_bits32(w, lane);
         zs = p.inv_keep;
       }
       uint32_t pk[16];
-      if (p.use_dropout) {
+      if constexpr (kDrop) {
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const float a = ((keep >> (2 * c)) & 1u) ? pr[2 * c] * zs : 0.f;
-          const float b = ((keep >> (2 * c + 1)) & 1u) ? pr[2 * c + 1] * zs : 0.f;
+          const float z0 = ((keep >> (2 * c)) & 1u) ? zs : 0.f;
+          const float z1 = ((keep >> (2 * c + 1)) & 1u) ? zs : 0.f;
+          float a, b;
+          mul2(a, b, pr[2 * c], pr[2 * c + 1], z0, z1);
           pk[c] = pack2<kBF16>(a, b);
         }
       } else {
@@ -533,13 +607,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const float4 d4 = ld_shared_f4(dsum_addr + 16 * c4);
           const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
           float ds[4];
-          if (p.use_dropout) {
+          if constexpr (kDrop) {
+            // dS = P (dP Z / keep_prob - D)
+            float z[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c = 4 * c4 + e;
-              const float z = ((keep >> c) & 1u) ? zs : 0.f;
-              ds[e] = pr[c] * (__uint_as_float(rdp[c]) * z - dv[e]);
-            }
+            for (int e = 0; e < 4; ++e) z[e] = ((keep >> (4 * c4 + e)) & 1u) ? zs : 0.f;
+            fma2(ds[0], ds[1], __uint_as_float(rdp[4 * c4]), __uint_as_float(rdp[4 * c4 + 1]),
+                 z[0], z[1], -dv[0], -dv[1]);
+            fma2(ds[2], ds[3], __uint_as_float(rdp[4 * c4 + 2]),
+                 __uint_as_float(rdp[4 * c4 + 3]), z[2], z[3], -dv[2], -dv[3]);
+            mul2(ds[0], ds[1], ds[0], ds[1], pr[4 * c4], pr[4 * c4 + 1]);
+            mul2(ds[2], ds[3], ds[2], ds[3], pr[4 * c4 + 2], pr[4 * c4 + 3]);
           } else {
             sub2(ds[0], ds[1], __uint_as_float(rdp[4 * c4]), __uint_as_float(rdp[4 * c4 + 1]),
                  dv[0], dv[1]);
@@ -568,19 +646,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (lane == 0) mbar_arrive(bar(B_DSFULL));
     }
     // ------------------------------------------------------------ epilogue
+    // dV is complete once the last dV product has run (the last PFREE
+    // commit), while that tile's dK and dQ^T products may still run: the dV
+    // half starts then; the dK half waits for all products (B_ACC).
     bool have = n_it > 0 && !*reinterpret_cast<volatile int *>(&s_abort);
-    if (have) have = wait_or_abort(ctl, bar(B_ACC), 0, ROLE_EPILOGUE);
+    if (have)
+      have = half == 0 ? wait_or_abort(ctl, bar(B_PFREE), (n_it - 1) & 1, ROLE_EPILOGUE)
+                       : wait_or_abort(ctl, bar(B_ACC), 0, ROLE_EPILOGUE);
     tc_fence_after();
     // A full key tile goes out through shared memory and two bulk tensor
-    // stores per tensor (dV staged in the idle Q stages, dK in the dY
-    // stages, as two [128 x 64] boxes in the 128-byte swizzle); the last,
+    // stores per tensor (dV staged in the dY stages, which no product reads
+    // after the last dV; dK in the Q stages, idle once every product has
+    // run; two [128 x 64] boxes each in the 128-byte swizzle); the last,
     // partial tile of a sequence is stored row by row, so that no row of
     // the next sequence is touched.
     const bool tile_full = k0 + BN <= sq.len_k;
     if (tile_full && (n_it == 0 || have)) {
       const float sc = half == 0 ? 1.f : p.scale;
       const uint32_t col = half == 0 ? COL_DV : COL_DK;
-      const uint32_t stage = sb + (half == 0 ? SM_Q : SM_DY);
+      const uint32_t stage = sb + (half == 0 ? SM_DY : SM_Q);
 #pragma unroll 1
       for (int c0 = 0; c0 < DD * nh; c0 += 32) {
         uint32_t r[32];
@@ -646,7 +730,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
     }
-  } else if (warp >= 12) {
+  } else {
     // ------------------------------------------------------------ dQ drain
     const int quarter = warp & 3;
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
@@ -788,7 +872,7 @@ bool make_map(CUtensorMap *m, const void *base, int64_t rows, int heads, int d, 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kBF16, bool kDet, bool kMask, bool kD64>
+template <bool kBF16, bool kDet, bool kMask, bool kD64, bool kDrop>
 cudaError_t launch_t(const BwdParams &p, cudaStream_t st) {
   const int d = kD64 ? 64 : HD;
   TcMaps maps{};
@@ -819,8 +903,8 @@ cudaError_t launch_t(const BwdParams &p, cudaStream_t st) {
       q.am_tma = 1;
     }
   }
-  const uint32_t smem = kMask ? SMEM_BYTES_MASK : SMEM_BYTES;
-  cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<kBF16, kDet, kMask, kD64>,
+  const uint32_t smem = kMask ? smem_bytes_mask(kDrop) : smem_bytes(kDrop);
+  cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<kBF16, kDet, kMask, kD64, kDrop>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   int dev = 0;
@@ -828,22 +912,26 @@ cudaError_t launch_t(const BwdParams &p, cudaStream_t st) {
   if ((e = cudaDeviceGetAttribute(&q.prefetch_ahead, cudaDevAttrMultiProcessorCount, dev)) !=
       cudaSuccess)
     return e;
-  bwd_tc_kernel<kBF16, kDet, kMask, kD64><<<p.n_items, NTHREADS, smem, st>>>(q, maps);
+  bwd_tc_kernel<kBF16, kDet, kMask, kD64, kDrop><<<p.n_items, NTHREADS, smem, st>>>(q, maps);
   return cudaGetLastError();
 }
 
-template <bool kBF16, bool kD64>
+template <bool kBF16, bool kD64, bool kDrop>
 cudaError_t launch_dd(const BwdParams &p, cudaStream_t s) {
   const bool mask = p.atten_mask != nullptr;
   if (p.deterministic)
-    return mask ? launch_t<kBF16, true, true, kD64>(p, s) : launch_t<kBF16, true, false, kD64>(p, s);
-  return mask ? launch_t<kBF16, false, true, kD64>(p, s) : launch_t<kBF16, false, false, kD64>(p, s);
+    return mask ? launch_t<kBF16, true, true, kD64, kDrop>(p, s)
+                : launch_t<kBF16, true, false, kD64, kDrop>(p, s);
+  return mask ? launch_t<kBF16, false, true, kD64, kDrop>(p, s)
+              : launch_t<kBF16, false, false, kD64, kDrop>(p, s);
 }
 
 template <bool kBF16>
 cudaError_t launch_dt(const BwdParams &p, cudaStream_t s) {
-  if (p.d == 64) return launch_dd<kBF16, true>(p, s);
-  if (p.d == HD) return launch_dd<kBF16, false>(p, s);
+  if (p.d == 64)
+    return p.use_dropout ? launch_dd<kBF16, true, true>(p, s) : launch_dd<kBF16, true, false>(p, s);
+  if (p.d == HD)
+    return p.use_dropout ? launch_dd<kBF16, false, true>(p, s) : launch_dd<kBF16, false, false>(p, s);
   return cudaErrorInvalidValue;
 }
 

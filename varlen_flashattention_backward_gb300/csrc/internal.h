@@ -70,12 +70,18 @@ struct BwdParams {
   int32_t *err;
   // Deterministic mode: CTAs take items in ticket order (*ticket counts up
   // from 0) and add their dQ partials of (query head n, padded query tile g)
-  // in ascending key-tile order.  sem[n * (tp / 64) + g] counts the partials
-  // already added; qfirst[g] is the first key tile that visits tile g.
+  // in descending key-tile order.  sem[n * (tp / 64) + g] (zeroed by the
+  // preprocess) counts the partials already added; qfirst[g] is the first
+  // key tile in that order (the highest that visits tile g).
   int deterministic;
   int32_t *ticket;
   int32_t *sem;
   const int32_t *qfirst;
+  // Dropout with every 128-key tile of every keep-mask row starting on a
+  // 16-byte boundary (all key lengths multiples of 128, mask 16-byte
+  // aligned): the tensor-core kernel copies each stage's keep bits into
+  // shared memory beside Q and dY.
+  int drop_rows16;
   int n_items, batch, n, n_kv, d, tp, total_q, total_kv;
   int prefetch_ahead;   // tcgen05 kernel: item distance of the K/V L2 prefetch (the SM count)
   float scale, scale_log2, inv_keep;

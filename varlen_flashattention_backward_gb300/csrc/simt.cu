@@ -18,8 +18,13 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
 // preprocess: D_i = sum_d dY * Y, lse2_i = (max_i + ln sum_i) * log2(e),
-// dq_acc row := 0.  One block per (64-row padded query tile, head).
+// dq_acc row := 0, the tile's deterministic-mode dQ counter := 0.  One block
+// per (64-row padded query tile, head).
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void clear_dq_counter(const BwdParams &p, int tile, int n) {
+  if (threadIdx.x == 0) p.sem[int64_t(n) * (p.tp / kQTile) + tile] = 0;
+}
+
 template <typename T>
 __device__ __forceinline__ float dot16(uint4 a, uint4 b) {
   const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
@@ -60,6 +65,7 @@ __global__ void __launch_bounds__(256) preprocess_vec_kernel(BwdParams p) {
   const int sub = lane / kLanes, part = lane % kLanes;
   const uint4 *dy = static_cast<const uint4 *>(p.dy);
   const uint4 *y = static_cast<const uint4 *>(p.y);
+  clear_dq_counter(p, tile, n);
   for (int e = threadIdx.x; e < kQTile * (D / 4); e += 256) {
     const int r = e / (D / 4), c4 = e % (D / 4);
     const int i = row0 + r - s.qpad;
@@ -116,6 +122,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(BwdParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const T *dy = static_cast<const T *>(p.dy);
   const T *y = static_cast<const T *>(p.y);
+  clear_dq_counter(p, tile, n);
   for (int r = warp; r < kQTile; r += 8) {
     const int prow = row0 + r;
     const int i = prow - s.qpad;
