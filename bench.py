@@ -515,7 +515,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
-    ap.add_argument("--workload", type=int, default=3, choices=list(range(1, 13)))
+    ap.add_argument("--workload", type=int, default=3, choices=list(range(1, 15)))
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tcgen05"])
     ap.add_argument("--ref-budget", type=float, default=10.0,
                     help="seconds of oracle work per timed sample")

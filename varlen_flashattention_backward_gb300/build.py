@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "_build")
 LIB_NAME = "libfavarlen.so"
-SOURCES = ["abi.cpp", "simt.cu", "bwd_sm103.cu", "static_scratch.cu"]
+SOURCES = ["abi.cpp", "simt.cu", "bwd_sm103.cu", "bwd_sm103_pad.cu", "static_scratch.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

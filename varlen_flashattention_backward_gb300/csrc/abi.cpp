@@ -614,8 +614,8 @@ fa_status fa_varlen_bwd_ex(const void *q, const void *k, const void *v, const vo
   const int tile = impl == FA_BWD_TCGEN05 ? kTcKvTile : kSimtKvTile;
   const bool det = options && options->deterministic != 0;
   auto seqs = build_seqs(pr);
-  // The tensor-core kernel takes two kv heads per item at head dim 64.
-  const bool pairs = impl == FA_BWD_TCGEN05 && head_dim == 64 && !det;
+  // The tensor-core kernel takes two kv heads per item at head dim 64 and below.
+  const bool pairs = impl == FA_BWD_TCGEN05 && head_dim <= 64 && !det;
   auto items = build_bwd_items(pr, tile, det, device_attr(cudaDevAttrL2CacheSize), pairs,
                                2 * device_attr(cudaDevAttrMultiProcessorCount));
   // The deterministic mode's add order of each query tile.

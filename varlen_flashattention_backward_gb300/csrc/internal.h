@@ -114,6 +114,8 @@ struct FwdParams {
 cudaError_t launch_bwd_preprocess(const BwdParams &p, fa_dtype dt, cudaStream_t s);
 cudaError_t launch_bwd_simt(const BwdParams &p, fa_dtype dt, cudaStream_t s);
 cudaError_t launch_bwd_tcgen05(const BwdParams &p, fa_dtype dt, cudaStream_t s);
+// Head dims below the tensor-core kernel's compute width (32, 96).
+cudaError_t launch_bwd_tcgen05_pad(const BwdParams &p, fa_dtype dt, cudaStream_t s);
 cudaError_t launch_dq_convert(const BwdParams &p, fa_dtype dt, cudaStream_t s);
 cudaError_t launch_fwd_simt(const FwdParams &p, fa_dtype dt, cudaStream_t s);
 cudaError_t launch_gen_keep_mask(uint8_t *mask, int64_t nbits, uint64_t seed,

@@ -164,6 +164,12 @@ def workload(cid: int, seed: int = 0) -> Workload:
         # an explicit mask (sparseMode 1), 30% of the pairs excluded
         return Workload(12, "bf16", bench_lens, 16, 128, UNBOUNDED, UNBOUNDED, seed=seed,
                         sparse_mode=1, mask_density=0.3)
+    if cid == 13:
+        # head dim 96 (zero-padded to 128 on the tensor cores)
+        return Workload(13, "bf16", bench_lens, 16, 96, UNBOUNDED, 0, seed=seed)
+    if cid == 14:
+        # head dim 32 (zero-padded to 64 on the tensor cores)
+        return Workload(14, "bf16", bench_lens, 32, 32, UNBOUNDED, 0, seed=seed)
     raise ValueError(f"unknown workload {cid}")
 
 
