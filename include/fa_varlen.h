@@ -103,8 +103,10 @@ typedef enum {
 typedef enum { FA_DTYPE_FP32 = 0, FA_DTYPE_FP16 = 1, FA_DTYPE_BF16 = 2 } fa_dtype;
 
 /* Backward kernel choice (fa_varlen_bwd_ex).  AUTO picks the tcgen05
- * tensor-core kernel for 16-bit types and the fp32 CUDA-core kernel for
- * FLOAT32; SIMT forces the CUDA-core kernel for any type. */
+ * tensor-core kernel for 16-bit types at head dims 32, 64, 96 and 128 (32
+ * and 96 run zero-padded to 64 and 128) and the CUDA-core kernel otherwise
+ * (FLOAT32, head dim 192); SIMT forces the CUDA-core kernel for any type;
+ * TCGEN05 on a case it does not cover is FA_ERR_UNSUPPORTED. */
 typedef enum { FA_BWD_AUTO = 0, FA_BWD_SIMT = 1, FA_BWD_TCGEN05 = 2 } fa_bwd_impl;
 
 typedef struct {
@@ -321,8 +323,8 @@ fa_status fa_gen_keep_mask(uint8_t *mask, int64_t nbits, uint64_t seed,
  * ordered by their longest item.  The backward launches the same items in
  * this order, except that it sorts the last two waves (2 x SM count items)
  * longest first, or the whole list when Q, dY, K, V and the fp32 dQ
- * accumulator together fit in 85% of the device's L2; at head dim 64 the
- * tensor-core kernel also pairs adjacent kv heads.  An item means
+ * accumulator together fit in 85% of the device's L2; at head dims 64 and
+ * below the tensor-core kernel also pairs adjacent kv heads.  An item means
  * key rows [tile*kv_tile, tile*kv_tile + kv_tile) of that sequence and head
  * visit query tiles of 64 rows [lo, lo + count) of every query head of the
  * group.  kv_tile is 64 (CUDA-core kernel) or 128 (tcgen05 kernel).
