@@ -656,6 +656,9 @@ fa_status fa_varlen_bwd_ex(const void *q, const void *k, const void *v, const vo
   p.scale = float(scale);
   p.scale_log2 = float(scale * 1.4426950408889634);
   p.inv_keep = float(1.0 / keep_prob);
+  const bool fold = dropout && impl == FA_BWD_TCGEN05;
+  p.lse2_shift = fold ? float(std::log2(keep_prob)) : 0.f;
+  p.dsum_scale = fold ? float(keep_prob) : 1.f;
   p.use_dropout = dropout;
   p.timeout_ns = (options && options->wait_timeout_ns > 0) ? options->wait_timeout_ns
                                                            : kDefaultTimeoutNs;

@@ -346,9 +346,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // 32-column S, dP and P rows are the kernel's largest live set; the drain
   // group keeps the launch's 128.  The split stays within the 512 x 128
   // registers the block was launched with: 4 warps x 32 x 72 + 8 x 32 x 152
-  // + 4 x 32 x 128 = 64512.
+  // + 4 x 32 x 128 = 64512; at compute width 64 (whose issuers need fewer)
+  // 4 x 32 x 56 + 8 x 32 x 160 + 4 x 32 x 128 = 64512.
   if (warp < 4) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
+  if constexpr (kD64)
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+  else
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // The whole warp runs this loop; copies are issued by one elected lane.
@@ -527,7 +531,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   }
   } else if (warp < 12) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 152;");
+    if constexpr (kD64)
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 160;");
+    else
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 152;");
     // ------------------------------------------------------------ softmax / dS
     const int half = (warp - 4) >> 2;
     const int quarter = warp & 3;
@@ -590,7 +597,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
       uint32_t keep = 0xFFFFFFFFu;
-      float zs = 1.f;
       if constexpr (kDrop) {
         const int il = i0 + lane;
         uint32_t w = 0;
@@ -605,18 +611,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
         }
         keep = transpose_bits32(w, lane);
-        zs = p.inv_keep;
       }
       uint32_t pk[16];
       if constexpr (kDrop) {
+        // With dropout the preprocess has put log2(keep_prob) into lse2 and
+        // keep_prob into dsum, so pr is P / keep_prob.  A dropped entry is
+        // zero in the P^T operand and (below) in dP^T, after which
+        // dS = (P / keep_prob) (dP Z - keep_prob D) = P (dP Z / keep_prob - D)
+        // is the dropout-free expression.
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float z0 = ((keep >> (2 * c)) & 1u) ? zs : 0.f;
-          const float z1 = ((keep >> (2 * c + 1)) & 1u) ? zs : 0.f;
-          float a, b;
-          mul2(a, b, pr[2 * c], pr[2 * c + 1], z0, z1);
-          pk[c] = pack2<kBF16>(a, b);
-        }
+        for (int c = 0; c < 16; ++c)
+          pk[c] = pack2<kBF16>(((keep >> (2 * c)) & 1u) ? pr[2 * c] : 0.f,
+                               ((keep >> (2 * c + 1)) & 1u) ? pr[2 * c + 1] : 0.f);
       } else {
 #pragma unroll
         for (int c = 0; c < 16; ++c) pk[c] = pack2<kBF16>(pr[2 * c], pr[2 * c + 1]);
@@ -635,26 +641,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 d4 = ld_shared_f4(dsum_addr + 16 * c4);
           const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-          float ds[4];
           if constexpr (kDrop) {
-            // dS = P (dP Z / keep_prob - D)
-            float z[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) z[e] = ((keep >> (4 * c4 + e)) & 1u) ? zs : 0.f;
-            fma2(ds[0], ds[1], __uint_as_float(rdp[4 * c4]), __uint_as_float(rdp[4 * c4 + 1]),
-                 z[0], z[1], -dv[0], -dv[1]);
-            fma2(ds[2], ds[3], __uint_as_float(rdp[4 * c4 + 2]),
-                 __uint_as_float(rdp[4 * c4 + 3]), z[2], z[3], -dv[2], -dv[3]);
-            mul2(ds[0], ds[1], ds[0], ds[1], pr[4 * c4], pr[4 * c4 + 1]);
-            mul2(ds[2], ds[3], ds[2], ds[3], pr[4 * c4 + 2], pr[4 * c4 + 3]);
-          } else {
-            sub2(ds[0], ds[1], __uint_as_float(rdp[4 * c4]), __uint_as_float(rdp[4 * c4 + 1]),
-                 dv[0], dv[1]);
-            sub2(ds[2], ds[3], __uint_as_float(rdp[4 * c4 + 2]),
-                 __uint_as_float(rdp[4 * c4 + 3]), dv[2], dv[3]);
-            mul2(ds[0], ds[1], ds[0], ds[1], pr[4 * c4], pr[4 * c4 + 1]);
-            mul2(ds[2], ds[3], ds[2], ds[3], pr[4 * c4 + 2], pr[4 * c4 + 3]);
+            for (int e = 0; e < 4; ++e)
+              if (!((keep >> (4 * c4 + e)) & 1u)) rdp[4 * c4 + e] = 0u;
           }
+          float ds[4];
+          sub2(ds[0], ds[1], __uint_as_float(rdp[4 * c4]), __uint_as_float(rdp[4 * c4 + 1]),
+               dv[0], dv[1]);
+          sub2(ds[2], ds[3], __uint_as_float(rdp[4 * c4 + 2]), __uint_as_float(rdp[4 * c4 + 3]),
+               dv[2], dv[3]);
+          mul2(ds[0], ds[1], ds[0], ds[1], pr[4 * c4], pr[4 * c4 + 1]);
+          mul2(ds[2], ds[3], ds[2], ds[3], pr[4 * c4 + 2], pr[4 * c4 + 3]);
           pk[2 * c4] = pack2<kBF16>(ds[0], ds[1]);
           pk[2 * c4 + 1] = pack2<kBF16>(ds[2], ds[3]);
         }

@@ -64,8 +64,8 @@ struct BwdParams {
   void *dq, *dk, *dv;
   const SeqInfo *seqs;
   const WorkItem *items;
-  float *lse2;      // [N][Tp]  (max + ln sum) * log2(e); +inf for padding rows
-  float *dsum;      // [N][Tp]  sum_d dY * Y;               0 for padding rows
+  float *lse2;      // [N][Tp]  (max + ln sum) * log2(e) + lse2_shift; +inf for padding rows
+  float *dsum;      // [N][Tp]  dsum_scale * sum_d dY * Y;  0 for padding rows
   float *dq_acc;    // [Tq][N][D] fp32 accumulator of dS K (unscaled)
   int32_t *err;
   // Deterministic mode: CTAs take items in ticket order (*ticket counts up
@@ -85,6 +85,10 @@ struct BwdParams {
   int n_items, batch, n, n_kv, d, tp, total_q, total_kv;
   int prefetch_ahead;   // tcgen05 kernel: item distance of the K/V L2 prefetch (the SM count)
   float scale, scale_log2, inv_keep;
+  // Folded into lse2 and dsum by the preprocess: 0 and 1, except for the
+  // tensor-core kernel with dropout, which takes log2(keep_prob) and
+  // keep_prob (its exponentials then give P / keep_prob directly).
+  float lse2_shift, dsum_scale;
   int use_dropout;
   long long timeout_ns;
   // Explicit attention mask (uint8 [am_rows][am_cols], 1 = excluded) at

@@ -17,7 +17,9 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
-// preprocess: D_i = sum_d dY * Y, lse2_i = (max_i + ln sum_i) * log2(e),
+// preprocess: D_i = sum_d dY * Y, lse2_i = (max_i + ln sum_i) * log2(e)
+// (the tensor-core kernel with dropout takes D_i * keep_prob and
+// lse2_i + log2(keep_prob): BwdParams::dsum_scale, lse2_shift),
 // dq_acc row := 0, the tile's deterministic-mode dQ counter := 0.  One block
 // per (64-row padded query tile, head).
 // ---------------------------------------------------------------------------
@@ -102,7 +104,8 @@ __global__ void __launch_bounds__(256) preprocess_vec_kernel(BwdParams p) {
       float lse2 = CUDART_INF_F;
       if (i < s.len_q) {
         const float m = mm[k], l = ll[k];
-        if (l > 0.f && m > -CUDART_INF_F) lse2 = (m + logf(l)) * kLog2e;
+        if (l > 0.f && m > -CUDART_INF_F) lse2 = (m + logf(l)) * kLog2e + p.lse2_shift;
+        acc *= p.dsum_scale;
       } else {
         acc = 0.f;
       }
@@ -135,10 +138,10 @@ __global__ void __launch_bounds__(256) preprocess_kernel(BwdParams p) {
       for (int d = lane; d < D; d += 32) acc += to_f(dy[base + d]) * to_f(y[base + d]);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      dsum = acc;
+      dsum = acc * p.dsum_scale;
       const float m = p.smax[(t * p.n + n) * 8];
       const float l = p.ssum[(t * p.n + n) * 8];
-      if (l > 0.f && m > -CUDART_INF_F) lse2 = (m + logf(l)) * kLog2e;
+      if (l > 0.f && m > -CUDART_INF_F) lse2 = (m + logf(l)) * kLog2e + p.lse2_shift;
       float4 *acc_row = reinterpret_cast<float4 *>(p.dq_acc + base);
       for (int d4 = lane; d4 < D / 4; d4 += 32) acc_row[d4] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
