@@ -32,7 +32,8 @@
 //   1      MMA issuer for S^T and dP^T (k-steps interleaved); owns the TMEM
 //          allocation
 //   2      MMA issuer for dV, then dK interleaved with dQ^T
-//   3      idle
+//   3      deterministic mode: publishes each tile's dQ counter once the
+//          drain's reductions are visible GPU-wide; idle otherwise
 //   4-11   softmax: TMEM lane quarter = warp % 4 (one key per thread), column
 //          half = (warp - 4) / 4 (32 of the 64 queries); P, dropout, dS; then
 //          the dV (first half) / dK (second half) epilogue
@@ -103,7 +104,7 @@ static_assert(smem_bytes_mask(true) <= 232448, "shared memory per CTA");
 enum : int {
   B_KV = 0, B_FULL = 1, B_EMPTY = B_FULL + STAGES, B_SDFULL = B_EMPTY + STAGES, B_SDFREE,
   B_PFULL, B_PFREE, B_DSFULL, B_DSFREE, B_DQFULL, B_DQFREE, B_ACC, B_FINAL, B_FINAL_A,
-  B_EPI, B_COUNT = B_EPI + 2
+  B_EPI, B_DQPUB = B_EPI + 2, B_PUBFREE, B_COUNT   // B_DQPUB, B_PUBFREE: deterministic mode
 };
 static_assert(B_COUNT * 8 <= 256, "barrier area");
 
@@ -155,6 +156,15 @@ __device__ __forceinline__ uint32_t transpose_bits32(uint32_t w, int lane) {
                    : ((w & masks[k]) | ((o & masks[k]) << s));
   }
   return w;
+}
+
+// Mask of a packed pair: each 16-bit half all ones where its keep bit is set.
+// Bits c and 16 + c of `keep` (the pair's two queries) go to bits 15 and 31,
+// whose signs then fill the halves.
+__device__ __forceinline__ uint32_t pair_mask(uint32_t keep, int c) {
+  uint32_t m;
+  asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(m) : "r"(keep << (15 - c)));
+  return m;
 }
 
 template <bool kBF16>
@@ -312,6 +322,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(bar(B_FINAL_A), 1);
     mbar_init(bar(B_EPI), 4);       // epilogue: the four warps of the dV half
     mbar_init(bar(B_EPI + 1), 4);   // ... and of the dK half
+    mbar_init(bar(B_DQPUB), 128);
+    mbar_init(bar(B_PUBFREE), 1);
     mbar_fence_init();
   }
   if (warp == 1) {
@@ -529,6 +541,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_wait(bar(B_FINAL), 0, drain_ns, &never);
       }
     }
+  } else if (kDet) {
+    // ------------------------------------------------------------ dQ publisher
+    // Deterministic mode: once the four drain warps have issued a tile's dQ
+    // reductions and arrived on B_DQPUB (release at CTA scope), this warp's
+    // GPU-scope fence makes them visible before the tile's counter moves on
+    // (the fence is cumulative over what the mbarrier wait has observed),
+    // so the next key tile in the add order cannot add first.  The drain
+    // goes on to its next tile meanwhile; B_PUBFREE keeps it at most one
+    // tile ahead of this warp.
+    for (int L = 0; L < n_it; ++L) {
+      const int n = kvh * group + L / qcnt;
+      const int qt = qlo + L % qcnt;
+      if (!wait_or_abort(ctl, bar(B_DQPUB), L & 1, ROLE_DQ)) break;
+      if (lane == 0) {
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
+        st_release_gpu(dq_counter(p, sq, n, qt), dq_rank(p, sq, item.tile, qt) + 1);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_PUBFREE));
+    }
   }
   } else if (warp < 12) {
     if constexpr (kD64)
@@ -598,11 +630,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       uint32_t keep = 0xFFFFFFFFu;
       if constexpr (kDrop) {
-        const int il = i0 + lane;
+        // Lane l reads query 2l (l < 16) or 2(l - 16) + 1: after the transpose
+        // bit c of keep is query 2c and bit 16 + c query 2c + 1.
+        const int ql = lane < 16 ? 2 * lane : 2 * lane - 31;
+        const int il = i0 + ql;
         uint32_t w = 0;
         if (il < sq.len_q) {
           if (p.drop_rows16) {
-            w = ld_shared_u32(sb + SM_DROP + st * DROP_STAGE + (32 * half + lane) * 16 +
+            w = ld_shared_u32(sb + SM_DROP + st * DROP_STAGE + (32 * half + ql) * 16 +
                               quarter * 4);
           } else {
             const int64_t bit = sq.mask_off + (int64_t(n) * sq.len_q + il) * sq.len_k + k0 +
@@ -615,14 +650,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       uint32_t pk[16];
       if constexpr (kDrop) {
         // With dropout the preprocess has put log2(keep_prob) into lse2 and
-        // keep_prob into dsum, so pr is P / keep_prob.  A dropped entry is
-        // zero in the P^T operand and (below) in dP^T, after which
-        // dS = (P / keep_prob) (dP Z - keep_prob D) = P (dP Z / keep_prob - D)
-        // is the dropout-free expression.
+        // keep_prob into dsum, so pr is P / keep_prob and dv below is
+        // keep_prob D.  A dropped entry is zero in the P^T operand; its dS is
+        // -(P / keep_prob)(keep_prob D) = -P D, a kept one's the dropout-free
+        // expression (P / keep_prob)(dP - keep_prob D) = P (dP / keep_prob - D).
+        // Both are packed and the pair mask picks per bf16 half.
 #pragma unroll
         for (int c = 0; c < 16; ++c)
-          pk[c] = pack2<kBF16>(((keep >> (2 * c)) & 1u) ? pr[2 * c] : 0.f,
-                               ((keep >> (2 * c + 1)) & 1u) ? pr[2 * c + 1] : 0.f);
+          pk[c] = pack2<kBF16>(pr[2 * c], pr[2 * c + 1]) & pair_mask(keep, c);
       } else {
 #pragma unroll
         for (int c = 0; c < 16; ++c) pk[c] = pack2<kBF16>(pr[2 * c], pr[2 * c + 1]);
@@ -641,11 +676,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 d4 = ld_shared_f4(dsum_addr + 16 * c4);
           const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-          if constexpr (kDrop) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (!((keep >> (4 * c4 + e)) & 1u)) rdp[4 * c4 + e] = 0u;
-          }
           float ds[4];
           sub2(ds[0], ds[1], __uint_as_float(rdp[4 * c4]), __uint_as_float(rdp[4 * c4 + 1]),
                dv[0], dv[1]);
@@ -655,6 +685,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mul2(ds[2], ds[3], ds[2], ds[3], pr[4 * c4 + 2], pr[4 * c4 + 3]);
           pk[2 * c4] = pack2<kBF16>(ds[0], ds[1]);
           pk[2 * c4 + 1] = pack2<kBF16>(ds[2], ds[3]);
+          if constexpr (kDrop) {
+            float e[4];
+            mul2(e[0], e[1], pr[4 * c4], pr[4 * c4 + 1], -dv[0], -dv[1]);
+            mul2(e[2], e[3], pr[4 * c4 + 2], pr[4 * c4 + 3], -dv[2], -dv[3]);
+            const uint32_t m0 = pair_mask(keep, 2 * c4), m1 = pair_mask(keep, 2 * c4 + 1);
+            pk[2 * c4] = (pk[2 * c4] & m0) | (pack2<kBF16>(e[0], e[1]) & ~m0);
+            pk[2 * c4 + 1] = (pk[2 * c4 + 1] & m1) | (pack2<kBF16>(e[2], e[3]) & ~m1);
+          }
         }
       }
       if (L > 0 && !wait_or_abort(ctl, bar(B_DSFREE), (L - 1) & 1, ROLE_SOFTMAX)) break;
@@ -787,13 +825,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (lane == 0) mbar_arrive(bar(B_DQFREE));
       // Deterministic mode: wait until the key tiles before this one in the add
       // order (descending key tiles) have added their partials of this query tile
-      // (the counter holds how many have), add, then publish count + 1.
-      int32_t *ctr = nullptr;
-      int rank = 0;
+      // (the counter holds how many have), add; warp 3 then publishes count + 1.
       if constexpr (kDet) {
         const int qt = qlo + L % qcnt;
-        ctr = dq_counter(p, sq, n, qt);
-        rank = dq_rank(p, sq, item.tile, qt);
+        int32_t *ctr = dq_counter(p, sq, n, qt);
+        const int rank = dq_rank(p, sq, item.tile, qt);
         if (warp == 12 && lane == 0) {
           const bool got = wait_counter(ctr, rank, p.timeout_ns,
                                         reinterpret_cast<volatile int *>(&s_abort));
@@ -843,9 +879,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             red_add_v4_f32(ptr, out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
       }
       if constexpr (kDet) {
-        __threadfence();
-        drain_bar_sync();
-        if (warp == 12 && lane == 0) st_release_gpu(ctr, rank + 1);
+        // warp 3 publishes this tile (after the previous one)
+        if (L > 0 && !wait_or_abort(ctl, bar(B_PUBFREE), (L - 1) & 1, ROLE_DQ)) break;
+        mbar_arrive(bar(B_DQPUB));
       }
     }
   }
