@@ -13,8 +13,8 @@ L2 is flushed all the same (a 256 MB write) before every timed step, outside
 the timed region.  `--workload 2` (T = 4096, whose inputs fit in L2) and the
 others are extra lines.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5]
-                    [--impl reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..16]
+                    [--deterministic] [--impl reference]
 
 `--impl reference` times the fp64 CPU oracle on a bounded sample of the same
 workload instead (the only reference available: the pages ship no code).
@@ -515,7 +515,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
-    ap.add_argument("--workload", type=int, default=3, choices=list(range(1, 15)))
+    ap.add_argument("--workload", type=int, default=3, choices=list(range(1, 17)))
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tcgen05"])
     ap.add_argument("--ref-budget", type=float, default=10.0,
                     help="seconds of oracle work per timed sample")

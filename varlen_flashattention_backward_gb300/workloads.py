@@ -16,7 +16,9 @@ The five workloads are the ones the library is measured and checked on:
 
 Workload 6 is the profiling case: bf16, 8 x 2048 (T = 16384), N = 16,
 D = 128, causal.  Its inputs (335 MB) exceed L2 while one backward launch
-stays well under a millisecond.
+stays well under a millisecond.  Workloads 15 and 16 are workload 5 cut to
+2 x 8192 tokens (the same window and heads), with and without dropout: the
+dropout path's profiling pair (0.5 GB of inputs and keep bits).
 
 Every workload uses scale = 1/sqrt(D).  Q, K, V and dY are drawn in fp32
 from one ``torch.Generator`` seeded with ``seed`` (order: lengths when they
@@ -170,6 +172,11 @@ def workload(cid: int, seed: int = 0) -> Workload:
     if cid == 14:
         # head dim 32 (zero-padded to 64 on the tensor cores)
         return Workload(14, "bf16", bench_lens, 32, 32, UNBOUNDED, 0, seed=seed)
+    if cid in (15, 16):
+        # workload 5 cut to two sequences of 8192 tokens, with (15) and
+        # without (16) dropout
+        return Workload(cid, "bf16", [8192] * 2, 16, 128, 4096, 0,
+                        keep_prob=0.9 if cid == 15 else 1.0, seed=seed)
     raise ValueError(f"unknown workload {cid}")
 
 
