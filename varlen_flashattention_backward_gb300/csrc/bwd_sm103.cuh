@@ -159,11 +159,16 @@ __device__ __forceinline__ uint32_t transpose_bits32(uint32_t w, int lane) {
 }
 
 // Mask of a packed pair: each 16-bit half all ones where its keep bit is set.
-// Bits c and 16 + c of `keep` (the pair's two queries) go to bits 15 and 31,
-// whose signs then fill the halves.
-__device__ __forceinline__ uint32_t pair_mask(uint32_t keep, int c) {
+// Bits c and 16 + c of the keep word (the pair's two queries) are read from
+// ks[s] = keep << s (s = 0..7): pair c < 8 has them at bits 7 and 23 of
+// ks[7 - c], pair c >= 8 at bits 15 and 31 of ks[15 - c]; prmt then fills
+// each half with the sign of its byte.
+__device__ __forceinline__ uint32_t pair_mask8(const uint32_t (&ks)[8], int c) {
   uint32_t m;
-  asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(m) : "r"(keep << (15 - c)));
+  if (c < 8)
+    asm("prmt.b32 %0, %1, 0, 0xAA88;" : "=r"(m) : "r"(ks[7 - c]));
+  else
+    asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(m) : "r"(ks[15 - c]));
   return m;
 }
 
@@ -648,6 +653,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         keep = transpose_bits32(w, lane);
       }
       uint32_t pk[16];
+      uint32_t ks[8];   // shifted copies of keep for pair_mask8
+#pragma unroll
+      for (int s = 0; s < 8; ++s) ks[s] = keep << s;
       if constexpr (kDrop) {
         // With dropout the preprocess has put log2(keep_prob) into lse2 and
         // keep_prob into dsum, so pr is P / keep_prob and dv below is
@@ -657,7 +665,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // Both are packed and the pair mask picks per bf16 half.
 #pragma unroll
         for (int c = 0; c < 16; ++c)
-          pk[c] = pack2<kBF16>(pr[2 * c], pr[2 * c + 1]) & pair_mask(keep, c);
+          pk[c] = pack2<kBF16>(pr[2 * c], pr[2 * c + 1]) & pair_mask8(ks, c);
       } else {
 #pragma unroll
         for (int c = 0; c < 16; ++c) pk[c] = pack2<kBF16>(pr[2 * c], pr[2 * c + 1]);
@@ -689,7 +697,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             float e[4];
             mul2(e[0], e[1], pr[4 * c4], pr[4 * c4 + 1], -dv[0], -dv[1]);
             mul2(e[2], e[3], pr[4 * c4 + 2], pr[4 * c4 + 3], -dv[2], -dv[3]);
-            const uint32_t m0 = pair_mask(keep, 2 * c4), m1 = pair_mask(keep, 2 * c4 + 1);
+            const uint32_t m0 = pair_mask8(ks, 2 * c4), m1 = pair_mask8(ks, 2 * c4 + 1);
             pk[2 * c4] = (pk[2 * c4] & m0) | (pack2<kBF16>(e[0], e[1]) & ~m0);
             pk[2 * c4 + 1] = (pk[2 * c4 + 1] & m1) | (pack2<kBF16>(e[2], e[3]) & ~m1);
           }
