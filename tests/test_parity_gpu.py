@@ -185,6 +185,48 @@ def test_empty_queries_give_zero_key_gradients():
     assert float(dk.abs().max()) == 0.0 and float(dv.abs().max()) == 0.0
 
 
+# Rows whose window holds a single key: the softmax gives P = 1 there (Z /
+# keep_prob under dropout) and Y = P V_j, so dP = dY V_j^T and D = dY Y^T
+# agree and dS = P (dP Z / keep_prob - D) vanishes; dQ and dK are zero in
+# exact arithmetic and dV is the only nonzero gradient.  An error relative
+# to an all-zero reference means nothing, so dQ and dK are held to the
+# tolerance times the size of the terms that cancel.  The first case came
+# from a seeded random search: an outer split leaves one row with one key.
+SINGLE_KEY = {
+    "fp16_d32_gqa_dropout_split": (
+        wl.Workload(60, "fp16", [22], 4, 32, 86, 0, keep_prob=0.85, seed=526, mask_seed=24301,
+                    n_heads_kv=2), [86], [107]),
+    "bf16_d128_diagonal": (wl.Workload(61, "bf16", [200, 77], 2, 128, 0, 0, seed=61), None, None),
+    "bf16_d64_diagonal_dropout": (
+        wl.Workload(62, "bf16", [130, 64], 4, 64, 0, 0, keep_prob=0.8, seed=62, n_heads_kv=2),
+        None, None),
+}
+
+
+@pytest.mark.parametrize("impl", ["simt", "tcgen05"])
+@pytest.mark.parametrize("name", list(SINGLE_KEY))
+def test_single_key_rows(name, impl):
+    w, qs, ks = SINGLE_KEY[name]
+    impl_id = _impl_or_skip(impl, w)
+    tensors = wl.make_tensors(w)
+    mask = device_mask(w, DEV)
+    out = gpu_forward_backward(w, tensors, DEV, impl_id, mask, q_start=qs, kv_start=ks)
+    mask_np = None if mask is None else mask.cpu().numpy()
+    ref = oracle_full(w, tensors, mask_np, q_start=qs, kv_start=ks)
+    assert_close(out, ref, TOL[w.dtype], keys=("y", "dv"))
+    # |dS| terms: |dP| Z / keep_prob <= |dY| |V| / keep_prob, and |D| <= |dY| |Y|
+    # with |Y| <= max |V_j| / keep_prob; one key per row.
+    q, k, v, dy = (f64(t) for t in tensors)
+    norm = lambda x: float(np.sqrt((x * x).sum(-1)).max())
+    ds_terms = 2.0 * norm(dy) * norm(v) / w.keep_prob
+    bound = {"dq": w.scale * ds_terms * float(np.abs(k).max()),
+             "dk": w.scale * ds_terms * float(np.abs(q).max())}
+    for key in ("dq", "dk"):
+        assert float(np.abs(ref[key]).max()) <= 1e-9 * bound[key], key   # the premise
+        err = float(np.abs(f64(out[key]) - ref[key]).max())
+        assert err <= TOL[w.dtype] * bound[key], (key, err, bound[key])
+
+
 def test_keep_mask_generator_matches_cpu_twin():
     w = wl.workload(5)
     mask = fa.gen_keep_mask(w.mask_bits, w.mask_seed, w.keep_prob, device=DEV)
