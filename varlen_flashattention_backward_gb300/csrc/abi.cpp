@@ -288,7 +288,7 @@ void build_qtables(const Problem &pr, const std::vector<SeqInfo> &seqs,
   const size_t g_tiles = size_t(pr.tp / kQTile);
   std::vector<int32_t> lo(g_tiles, INT32_MAX), hi(g_tiles, -1), cnt(g_tiles, 0);
   for (const WorkItem &w : items) {
-    if (w.head != 0) continue;
+    if ((w.head & 0xFFFF) != 0) continue;   // the items of (the pair starting at) kv head 0
     const size_t g0 = size_t(seqs[size_t(w.seq)].qpad / kQTile) + size_t(item_lo(w));
     for (int t = 0; t < item_count(w); ++t) {
       lo[g0 + t] = std::min(lo[g0 + t], w.tile);
@@ -615,7 +615,7 @@ fa_status fa_varlen_bwd_ex(const void *q, const void *k, const void *v, const vo
   const bool det = options && options->deterministic != 0;
   auto seqs = build_seqs(pr);
   // The tensor-core kernel takes two kv heads per item at head dim 64 and below.
-  const bool pairs = impl == FA_BWD_TCGEN05 && head_dim <= 64 && !det;
+  const bool pairs = impl == FA_BWD_TCGEN05 && head_dim <= 64;
   auto items = build_bwd_items(pr, tile, det, device_attr(cudaDevAttrL2CacheSize), pairs,
                                2 * device_attr(cudaDevAttrMultiProcessorCount));
   // The deterministic mode's add order of each query tile.
